@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Benchmark of the 1-bit LAMB hot path on GB300.
+
+One step = one compression-stage step of the whole hot path (fused worker +
+server compression over all W workers, per-tensor factor, frozen-variance
+update) over the workload's full parameter table, through the C ABI.
+Gradients are regenerated on the device before every step, outside the
+CUDA-event-timed region (so every step sees new gradients and the L2 is
+flushed between steps: each step moves ~80 GB, far above the 129 MB L2).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workload  # noqa: E402  (seeded synthetic inputs; no optimizer arithmetic)
+
+METRIC = "compression-stage param elements/s per step and achieved HBM GB/s vs GB300 peak"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="large",
+                   choices=("tiny", "base", "large", "large_w32", "gpt2xl"))
+    p.add_argument("--max-params", type=int, default=0,
+                   help="keep only the leading tensors up to this many parameters (profiling)")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+def get_workload(args):
+    wl = workload.workloads()[args.workload]
+    if args.max_params:
+        keep, n = [], 0
+        for name, shape in wl.tensors:
+            size = int(np.prod(shape))
+            if keep and n + size > args.max_params:
+                break
+            keep.append((name, shape))
+            n += size
+        wl.tensors = keep
+        wl.name = f"{wl.name}[:{n}]"
+    return wl
+
+
+def grad_bytes(wl):
+    return {"f32": 4, "bf16": 2, "philox": 0}[wl.grad]
+
+
+def fused_kernel_bytes(wl):
+    """Algorithmic HBM bytes of one launch of the fused compression kernel:
+    per parameter W*(g + 4 + 4 + 1/8) + (4 m + 4 e_s + 4 v + 4 v_fresh) read and
+    (4 e_s + 4 m + 4 v_fresh + 1/8 signs) written; plus 4 bytes per scale."""
+    W = wl.W
+    per = W * (grad_bytes(wl) + 8.125) + 28.125
+    return wl.N * per + 4.0 * wl.K * (W + 1)
+
+
+def step_bytes(wl):
+    """Fused kernel + update kernel (m, v, x read, x written: 16 B/param)."""
+    return fused_kernel_bytes(wl) + 16.0 * wl.N
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    for f in ("k_compress.cu", "lamb1b_internal.cuh"):
+        with open(os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(workload_name):
+    """dram bytes per launch of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"compress_kernel_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+source_sha:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = os.path.join("/tmp", f"lamb1b_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.remove(self.out)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one replica per rank, weak scaling)
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(wl, seconds, max_steps=None):
+    """Times the oracle's compression step on the leading chunks of the
+    workload.  Returns (elements/s, description, steps)."""
+    import oracle
+    C, W = wl.chunk, wl.W
+
+    def make(nchunks):
+        n = min(nchunks * C, wl.N)
+        ends = wl.offsets + wl.numels
+        frags = []
+        for o, e in zip(wl.offsets, ends):
+            if o >= n:
+                break
+            frags.append((int(o), int(min(e, n) - o)))
+        x0 = workload.gen_params(wl, 0, n)
+        o = oracle.Oracle([f[0] for f in frags], [f[1] for f in frags], W, C, wl.hp, x0)
+        o.v[:] = 1e-6
+        o.freeze()
+        g = np.empty((W, n), np.float32)
+        for w in range(W):
+            g[w] = workload.gen_grads_range(wl, 10, w, 0, n)
+            if wl.grad == "bf16":
+                g[w] = workload.bf16_round(g[w])
+        return o, g, n
+
+    o, g, n = make(8)
+    t0 = time.perf_counter()
+    o.compress_step(g)
+    dt = time.perf_counter() - t0
+    target = min(2.0, seconds / 5) if max_steps is None else max(0.05, seconds / max(1, max_steps))
+    nchunks = int(max(1, min(wl.K, 8 * target / max(dt, 1e-6))))
+    o, g, n = make(nchunks)
+    times = []
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end and (max_steps is None or len(times) < max_steps):
+        t0 = time.perf_counter()
+        o.compress_step(g)
+        times.append(time.perf_counter() - t0)
+    rate = n / statistics.median(times)
+    desc = (f"oracle compression step on the leading {n} parameters ({nchunks} chunks of "
+            f"{C}, W={W}) of {wl.name}; median of {len(times)} steps")
+    return rate, desc, len(times), times
+
+
+def cpu_info():
+    model = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return f"{os.uname().machine} {model}".strip(), os.cpu_count()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = get_workload(args)
+    total = max(30.0, 2.0 * (args.steps + args.warmup))
+    per_step_budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    rate, desc, n, times = oracle_sample_rate(wl, seconds=per_step_budget * (args.steps + args.warmup),
+                                              max_steps=args.steps + args.warmup)
+    timed = times[args.warmup:] or times
+    ms = 1e3 * statistics.mean(timed)
+    value = rate
+    arch, ncpu = cpu_info()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": len(timed), "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "W": wl.W, "chunk": wl.chunk, "params": wl.N,
+                   "grads": wl.grad},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc, "host": arch, "host_cpus": ncpu},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    del total
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import communication_compressed_optimizer_gb300 as pkg
+
+    torch.cuda.set_device(local)
+    wl = get_workload(args)
+    N, W, C = wl.N, wl.W, wl.chunk
+    layers = list(zip(wl.offsets.tolist(), wl.numels.tolist()))
+
+    x = torch.empty(N, device="cuda")
+    pkg.gen_params(x, 0, N, wl.param_std, wl.seed)
+    opt = pkg.OneBitLamb(x, layers, W, C, **wl.hp)
+    if wl.grad == "philox":
+        g = pkg.PhiloxGrads(wl.seed, wl.layer_std, wl.layer_heavy, wl.heavy_scale)
+
+        def regen(t):
+            pass
+        ld = 0
+    else:
+        q = 8 if wl.grad == "bf16" else 4
+        ld = -(-N // q) * q
+        g = torch.empty((W, ld), dtype=torch.int16 if wl.grad == "bf16" else torch.float32,
+                        device="cuda")
+
+        def regen(t):
+            pkg.gen_grads(g, t, wl.seed, layers, wl.layer_std, None, wl.heavy_scale)
+
+    def new_events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+    # warmup stage (LAMB), timed per step for information
+    t = 0
+    warm_ms, warm_kernel_ms = [], []
+    for _ in range(wl.warmup_steps):
+        regen(t)
+        ev = new_events()
+        opt.set_trace_events(ev)
+        opt.warmup_step(g)
+        torch.cuda.synchronize()
+        warm_ms.append(ev[0].elapsed_time(ev[3]))
+        warm_kernel_ms.append(ev[0].elapsed_time(ev[1]))
+        t += 1
+    opt.freeze_variance()
+    for _ in range(args.warmup):
+        regen(t)
+        opt.compress_step(g)
+        t += 1
+    opt.set_trace_events(None)
+    torch.cuda.synchronize()
+    barrier(world)
+
+    # ---- timed region -------------------------------------------------------
+    events = [new_events() for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        regen(t)
+        opt.set_trace_events(events[i])
+        opt.compress_step(g)
+        t += 1
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    opt.set_trace_events(None)
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    kern_ms = [e[0].elapsed_time(e[1]) for e in events]
+    factor_ms = [e[1].elapsed_time(e[2]) for e in events]
+    upd_ms = [e[2].elapsed_time(e[3]) for e in events]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    ms_per_step = 1e3 * total_s / args.steps
+    value = world * N * args.steps / total_s
+
+    peak, peak_kind = measured_peaks()
+    kb = fused_kernel_bytes(wl)
+    k_avg = statistics.mean(kern_ms)
+    achieved = kb / (k_avg / 1e3) / 1e9
+    traffic = profiled_traffic(wl.name)
+
+    # ---- end to end through the public API with host buffers ----------------
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        e2e = run_e2e(args, opt, wl, g, regen, t, ld)
+        t += args.e2e_steps + 1
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "W": W, "chunk": C, "params": N, "tensors": wl.L,
+                   "grads": wl.grad, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (each step moves %.1f GB); gradients regenerated "
+                         "on the device between timed steps" % (step_bytes(wl) / 1e9),
+                   "timing": "CUDA events on the launching stream around each step"},
+        "roofline": {"bound": "hbm", "kernel": "k_compress (fused worker+server pass)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": traffic, "alg_bytes_per_launch": kb,
+                     "kernel_ms": k_avg},
+        "step": {"alg_bytes": step_bytes(wl), "hbm_gbs": step_bytes(wl) / (ms_per_step / 1e3) / 1e9,
+                 "frac_of_peak": step_bytes(wl) / (ms_per_step / 1e3) / 1e9 / peak,
+                 "kernel_ms": {"compress": k_avg, "factor": statistics.mean(factor_ms),
+                               "update": statistics.mean(upd_ms)},
+                 "ms_p10": float(np.percentile(step_ms, 10)),
+                 "ms_p50": float(np.percentile(step_ms, 50)),
+                 "ms_p90": float(np.percentile(step_ms, 90)),
+                 "worker_elements_per_s": W * value, "wall_s": wall},
+        "warmup_stage": {"ms_per_step": statistics.mean(warm_ms[1:] or warm_ms),
+                         "moments_kernel_ms": statistics.mean(warm_kernel_ms[1:] or warm_kernel_ms),
+                         "params_per_s": N / (statistics.mean(warm_ms[1:] or warm_ms) / 1e3)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, n, _ = oracle_sample_rate(wl, seconds=args.cpu_seconds)
+        arch, ncpu = cpu_info()
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": desc, "host": arch, "host_cpus": ncpu}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    opt.close()
+
+
+def run_e2e(args, opt, wl, g, regen, t, ld):
+    """Same metric through the public API with host buffers: every step
+    copies its gradients from pinned host memory and reads back the server's
+    compressed message (sign words and chunk scales)."""
+    import torch
+    st = opt.state()
+    words, scales = st["signs_s"], st["scale_s"]
+    out_w = torch.empty(words.shape, dtype=words.dtype, pin_memory=True)
+    out_s = torch.empty(scales.shape, dtype=scales.dtype, pin_memory=True)
+    h2d = 0
+    host = None
+    if wl.grad != "philox":
+        regen(t)
+        host = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+        host.copy_(g)
+        h2d = g.numel() * g.element_size()
+    d2h = words.numel() * 4 + scales.numel() * 4
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s0.record()
+    for _ in range(args.e2e_steps):
+        if host is not None:
+            g.copy_(host, non_blocking=True)
+        opt.compress_step(g)
+        out_w.copy_(words, non_blocking=True)
+        out_s.copy_(scales, non_blocking=True)
+    s1.record()
+    torch.cuda.synchronize()
+    sec = s0.elapsed_time(s1) / 1e3
+    return {"value": wl.N * args.e2e_steps / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "ms_per_step": 1e3 * sec / args.e2e_steps}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

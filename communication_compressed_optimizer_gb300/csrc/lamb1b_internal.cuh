@@ -1,0 +1,160 @@
+// Internal structures shared by the lamb1b translation units: the problem
+// description, the workspace layout, the gradient source, and the device
+// helpers every kernel uses (explicitly rounded binary32 arithmetic, the
+// warp-level pairwise tree, sign-word packing, layer lookup).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "philox.cuh"
+
+namespace lamb1b {
+
+constexpr int kGranule = 256;        // level-0 block of the canonical pairwise tree
+constexpr int kMaxChunkLayers = 64;  // per-chunk layer slots kept in shared memory
+
+struct Problem {
+    int64_t N;        // parameters
+    int64_t Np;       // K * C, padded vector length
+    int64_t K;        // chunks
+    int64_t words_ld; // Np / 32
+    int32_t L, W, C;
+    float lr, beta1, beta2, eps, wd;
+    float omega1, omega2;             // fl(1 - beta1), fl(1 - beta2)
+    float cmin, cmax, cema, one_m_cema;
+    float fmin, fmax, fthr_lo, fthr_hi; // fl(1 - thr), fl(1 + thr)
+    float inv_dummy;
+    int32_t check_finite;
+};
+
+// Device pointers into the caller's workspace.
+struct Dev {
+    float* m;         // [Np]
+    float* v;         // [Np]  second moment; frozen after the stage switch
+    float* v_fresh;   // [Np]
+    float* e_s;       // [Np]
+    float* e_w;       // [W][Np]
+    uint32_t* signs_w;// [W][words_ld]
+    uint32_t* signs_s;// [words_ld]
+    float* scale_w;   // [W][K]
+    float* scale_s;   // [K]
+    float* c_bar;     // [L]
+    float* r_prev;    // [L]
+    float* c_cur;     // [L]
+    float* gc;        // [L] fl(lr * c_cur)
+    float* R_last;    // [L]
+    float* Sx;        // [L]
+    float* Su;        // [L]
+    uint32_t* Rmax;   // [L] bit patterns of positive floats, max-reduced
+    int64_t* layer_off;  // [L]
+    int64_t* layer_end;  // [L] off + numel
+    int64_t* hbase;      // [L+1] first half-granule partial of each layer
+    int32_t* chunk_l0;   // [K] layer of the chunk's first element
+    int32_t* chunk_l1;   // [K] layer of the chunk's last element
+    float* part_x;       // [hbase[L]] warmup half-granule sums of x^2
+    float* part_u;       // [hbase[L]] warmup half-granule sums of u^2
+    uint32_t* flags;     // [4] bit 0: non-finite gradient seen
+};
+
+struct Grads {
+    int32_t kind;     // 0 f32, 1 bf16, 2 philox
+    const void* ptr;
+    int64_t ld;
+    uint64_t seed;
+    const float* layer_std;
+    const uint8_t* layer_heavy;
+    float heavy_scale;
+    uint32_t t;       // global step index (Philox counter word 2)
+};
+
+enum { kGradF32 = 0, kGradBF16 = 1, kGradPhilox = 2 };
+
+// ---- explicitly rounded binary32 arithmetic --------------------------------
+__device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float fdiv(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ float fsqrt(float a) { return __fsqrt_rn(a); }
+// clip(x, a, b) = min{max{x, a}, b} by comparisons (a NaN x passes through)
+__device__ __forceinline__ float clip(float x, float a, float b)
+{
+    const float r = (x < a) ? a : x;
+    return (r > b) ? b : r;
+}
+
+// Pairwise tree of the 128 leaves held by a warp, 4 consecutive leaves per
+// lane (lane l holds leaves 4l..4l+3): ((f0+f1)+(f2+f3)) then butterfly
+// partners 1, 2, 4, 8, 16.  Every lane returns the total.
+__device__ __forceinline__ float warp_tree128(float f0, float f1, float f2, float f3)
+{
+    float v = fadd(fadd(f0, f1), fadd(f2, f3));
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Pairwise tree over `n` consecutive 128-leaf partials red[0..n) (n a power
+// of two); every lane of the calling warp returns the total.  Partials past
+// n are +0, which leaves the tree's value unchanged.
+template <int NPART>
+__device__ __forceinline__ float tree_over_partials(const float* red, int lane)
+{
+    float v;
+    if constexpr (NPART <= 32) {
+        v = (lane < NPART) ? red[lane] : 0.0f;
+    } else {
+        constexpr int PER = NPART / 32;
+        float t[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) t[j] = red[lane * PER + j];
+#pragma unroll
+        for (int w = 1; w < PER; w <<= 1)
+#pragma unroll
+            for (int j = 0; j < PER; j += 2 * w) t[j] = fadd(t[j], t[j + w]);
+        v = t[0];
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Places bit k of the low byte of x at bit 4k.
+__device__ __forceinline__ uint32_t spread8(uint32_t x)
+{
+    x &= 0xFFu;
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    x = (x | (x << 3)) & 0x11111111u;
+    return x;
+}
+
+// The warp holds 128 consecutive elements, 4 per lane; p0..p3 are the sign
+// predicates of the lane's components.  Lanes 0..3 return sign word `lane`
+// of the block (element 32*lane + b at bit b); other lanes return 0.
+__device__ __forceinline__ uint32_t pack_signs128(bool p0, bool p1, bool p2, bool p3, int lane)
+{
+    const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, p0);
+    const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, p1);
+    const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, p2);
+    const uint32_t b3 = __ballot_sync(0xFFFFFFFFu, p3);
+    const int sh = 8 * (lane & 3);
+    return spread8(b0 >> sh) | (spread8(b1 >> sh) << 1) | (spread8(b2 >> sh) << 2) |
+           (spread8(b3 >> sh) << 3);
+}
+
+// ---- launchers (one translation unit each) ---------------------------------
+// `ev` is NULL or 4 events recorded before the first kernel and after each
+// of the three kernels of a step.
+cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float* x,
+                          cudaStream_t st, int first_warmup, const cudaEvent_t* ev);
+cudaError_t launch_freeze(const Problem& P, const Dev& D, cudaStream_t st);
+cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
+                            cudaStream_t st, const cudaEvent_t* ev);
+
+inline cudaError_t trace(const cudaEvent_t* ev, int i, cudaStream_t st)
+{
+    return ev ? cudaEventRecord(ev[i], st) : cudaSuccess;
+}
+cudaError_t launch_init_layers(const Problem& P, const Dev& D, cudaStream_t st);
+
+}  // namespace lamb1b

@@ -1,0 +1,171 @@
+"""GPU: on-device generator equals the host generator bit for bit;
+determinism; checkpoint/resume; non-finite detection; call-order errors."""
+import numpy as np
+import pytest
+import torch
+
+import communication_compressed_optimizer_gb300 as pkg
+import workload
+from communication_compressed_optimizer_gb300 import _abi
+from harness import Pair, device_grads, grad_ld, layers_of
+
+pytestmark = pytest.mark.gpu
+
+
+def test_device_generator_matches_host_generator():
+    t = workload.bert_tensors(1, 96, 384, 700) + [("odd", (7,))]
+    for grad, heavy in (("f32", 0), ("bf16", 0), ("f32", 3)):
+        wl = workload.custom("gen", t, W=5, chunk=256, grad=grad, grad_std=1e-3,
+                             fan_in_scaled=True, heavy_every=heavy, heavy_scale=2e-3)
+        ld = grad_ld(wl) + 8
+        dt = torch.int16 if grad == "bf16" else torch.float32
+        out = torch.zeros((wl.W, ld), dtype=dt, device="cuda")
+        for step in (0, 7):
+            pkg.gen_grads(out, step, wl.seed, layers_of(wl), wl.layer_std,
+                          wl.layer_heavy if heavy else None, wl.heavy_scale)
+            got = out.cpu().numpy()
+            for w in range(wl.W):
+                want = workload.gen_grads(wl, step, w, bf16_bits=(grad == "bf16"))
+                if grad == "bf16":
+                    np.testing.assert_array_equal(got[w, :wl.N].view(np.uint16), want)
+                else:
+                    np.testing.assert_array_equal(got[w, :wl.N].view(np.uint32), want.view(np.uint32))
+                assert not np.any(got[w, wl.N:])
+    # parameters, including a range that does not start on a multiple of 4
+    wl = workload.workloads()["tiny"]
+    x = torch.empty(wl.N - 5, device="cuda")
+    pkg.gen_params(x, 5, wl.N, wl.param_std, wl.seed)
+    np.testing.assert_array_equal(x.cpu().numpy().view(np.uint32),
+                                  workload.gen_params(wl, 5, wl.N).view(np.uint32))
+
+
+def test_device_philox_stream_many_counters():
+    """2^22 consecutive counters of one stream, device vs host."""
+    wl = workload.custom("one", [("a", (1 << 22,))], W=1, chunk=256, grad_std=1.0)
+    out = torch.empty((1, wl.N), device="cuda")
+    pkg.gen_grads(out, 3, 12345, layers_of(wl), wl.layer_std)
+    wl.seed = 12345
+    want = workload.gen_grads(wl, 3, 0)
+    np.testing.assert_array_equal(out.cpu().numpy()[0].view(np.uint32), want.view(np.uint32))
+
+
+def _bert_mini(W=4, chunk=1024):
+    t = workload.bert_tensors(1, 64, 256, 500) + [("extra", (5,))]
+    return workload.custom("bm", t, W=W, chunk=chunk, grad_std=1e-3)
+
+
+def _run_gpu_only(wl, n_warm, n_comp):
+    x = torch.from_numpy(workload.gen_params(wl)).cuda()
+    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    ld = grad_ld(wl)
+    t = 0
+    for _ in range(n_warm):
+        opt.warmup_step(device_grads(wl, t, ld))
+        t += 1
+    opt.freeze_variance()
+    for _ in range(n_comp):
+        opt.compress_step(device_grads(wl, t, ld))
+        t += 1
+    torch.cuda.synchronize()
+    return opt, x
+
+
+def test_bitwise_deterministic():
+    wl = _bert_mini(W=6, chunk=2048)
+    a, xa = _run_gpu_only(wl, 3, 4)
+    b, xb = _run_gpu_only(wl, 3, 4)
+    assert torch.equal(xa.view(torch.int32), xb.view(torch.int32))
+    assert torch.equal(a.workspace, b.workspace)
+
+
+def test_checkpoint_resume_is_bitwise():
+    wl = _bert_mini()
+    ld = grad_ld(wl)
+    ref, xr = _run_gpu_only(wl, 3, 6)
+    # interrupted run: 3 warmup + 2 compression steps, save, restore, 4 more
+    a, xa = _run_gpu_only(wl, 3, 2)
+    sa = a.state()
+    saved = {k: v.clone() for k, v in sa.items() if isinstance(v, torch.Tensor)}
+    counters = (sa["t"], sa["n_warmup"], sa["stage"])
+    x_saved = xa.clone()
+    del a
+    xb = x_saved.clone()
+    b = pkg.OneBitLamb(xb, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    sb = b.state()
+    for k, v in saved.items():
+        sb[k].copy_(v)
+    b.set_counters(*counters)
+    t = counters[0]
+    for _ in range(4):
+        b.compress_step(device_grads(wl, t, ld))
+        t += 1
+    torch.cuda.synchronize()
+    assert torch.equal(xb.view(torch.int32), xr.view(torch.int32))
+    sr = ref.state()
+    sb = b.state()
+    for k in ("m", "v", "v_fresh", "e_s", "e_w", "signs_w", "signs_s", "scale_w", "scale_s",
+              "r_prev", "c_cur", "c_bar"):
+        assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
+
+
+def test_nonfinite_gradients_are_flagged():
+    wl = _bert_mini()
+    x = torch.from_numpy(workload.gen_params(wl)).cuda()
+    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **dict(wl.hp, check_finite=1))
+    ld = grad_ld(wl)
+    g = device_grads(wl, 0, ld)
+    opt.warmup_step(g)
+    opt.check_status()                       # clean
+    g[1, 123] = float("nan")
+    opt.warmup_step(g)
+    with pytest.raises(pkg.Lamb1bError) as e:
+        opt.check_status()
+    assert e.value.code == _abi.ERR_NONFINITE
+    opt.check_status()                       # cleared
+    opt.freeze_variance()
+    g = device_grads(wl, 2, ld)
+    g[0, 7] = float("inf")
+    opt.compress_step(g)
+    with pytest.raises(pkg.Lamb1bError):
+        opt.check_status()
+
+
+def test_call_order_and_argument_errors():
+    wl = _bert_mini()
+    x = torch.from_numpy(workload.gen_params(wl)).cuda()
+    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    ld = grad_ld(wl)
+    g = device_grads(wl, 0, ld)
+    with pytest.raises(pkg.Lamb1bError) as e:
+        opt.compress_step(g)
+    assert e.value.code == _abi.ERR_STATE
+    with pytest.raises(pkg.Lamb1bError) as e:
+        opt.warmup_step(torch.zeros((wl.W, wl.N - 8), device="cuda"))   # ld < N
+    assert e.value.code == _abi.ERR_ARG
+    gbad = torch.zeros((wl.W, ld + 1), device="cuda")[:, :ld + 1]
+    with pytest.raises(pkg.Lamb1bError) as e:
+        opt.warmup_step(gbad)                    # ld*4 not a multiple of 16
+    assert e.value.code == _abi.ERR_ALIGN
+    opt.warmup_step(g)
+    opt.freeze_variance()
+    with pytest.raises(pkg.Lamb1bError) as e:
+        opt.freeze_variance()
+    assert e.value.code == _abi.ERR_STATE
+    with pytest.raises(pkg.Lamb1bError) as e:
+        opt.warmup_step(g)
+    assert e.value.code == _abi.ERR_STATE
+    # a failed check changed nothing: the step counter is still 1
+    assert opt.state()["t"] == 1
+    # host memory is not accepted as parameters (checked through the C ABI)
+    import ctypes
+    L = _abi.load()
+    h = pkg._hparams(wl.W, wl.chunk, dict(pkg.DEFAULT_HP))
+    arr = pkg._layers_array(layers_of(wl))
+    host = np.zeros(wl.N + 64, np.float32)
+    hp_ptr = (host.ctypes.data + 255) // 256 * 256
+    ws = torch.empty(pkg.workspace_bytes(layers_of(wl), wl.W, wl.chunk), dtype=torch.uint8,
+                     device="cuda")
+    ctx = ctypes.c_void_p()
+    rc = L.lamb1b_init(ctypes.byref(ctx), arr, len(arr), ctypes.byref(h), ctypes.c_void_p(hp_ptr),
+                       ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
+    assert rc == _abi.ERR_ARG and ctx.value is None

@@ -1,0 +1,93 @@
+"""GPU parity of the whole hot path against the CPU oracle, step by step, on
+seeded workloads that span many chunks with ragged tails (N not a multiple of
+4, 32 or C), misaligned tensor boundaries, every chunk size, every gradient
+storage, and the degenerate cases (one worker, one element, a chunk holding
+more tensors than the kernel keeps in shared memory)."""
+import numpy as np
+import pytest
+
+import workload
+from harness import Pair
+
+pytestmark = pytest.mark.gpu
+
+
+def bert_mini(W=8, chunk=2048, grad="f32", **kw):
+    t = workload.bert_tensors(2, 64, 256, 1000) + [("extra", (5,))]
+    return workload.custom("bert_mini", t, W=W, chunk=chunk, grad=grad, grad_std=1e-3, **kw)
+
+
+def run(wl, n_warm, n_comp, expect_bitwise=True):
+    p = Pair(wl)
+    diffs = 0
+    for i in range(n_warm):
+        p.warmup()
+        diffs += p.compare(f"warmup {i}")
+    p.freeze()
+    diffs += p.compare("freeze")
+    for i in range(n_comp):
+        p.compress()
+        diffs += p.compare(f"compress {i}")
+    if expect_bitwise:
+        assert diffs == 0, f"{diffs} float elements differ in some bit"
+    return p
+
+
+def test_tiny_workload_full_run():
+    """The toy workload as specified: 4 tensors, W=4, C=256, 5 warmup steps,
+    freeze, 5 compression steps."""
+    wl = workload.workloads()["tiny"]
+    run(wl, wl.warmup_steps, wl.compress_steps)
+
+
+def test_bert_mini_twenty_steps():
+    """BERT-shaped table (odd tensor offsets, N % 4 == 3), W=8, C=2048,
+    10 warmup + 10 compression steps: parameters after 20 steps."""
+    wl = bert_mini()
+    assert wl.N % 4 == 3
+    run(wl, 10, 10)
+
+
+@pytest.mark.parametrize("chunk", [256, 512, 1024, 4096, 8192])
+def test_every_chunk_size(chunk):
+    wl = bert_mini(W=3, chunk=chunk)
+    run(wl, 2, 3)
+
+
+def test_bf16_gradients():
+    t = workload.gpt2_tensors(2, 48, 192, 500, n_pos=64)
+    wl = workload.custom("gpt2_mini", t, W=8, chunk=8192, grad="bf16", grad_std=1e-3)
+    assert wl.N > 3 * wl.chunk
+    run(wl, 3, 4)
+
+
+def test_in_kernel_philox_gradients_with_heavy_tails():
+    """Gradients drawn inside the kernels (W=32), per-tensor std scaled by
+    1/sqrt(fan_in), every fifth tensor Student-t(3)."""
+    t = workload.bert_tensors(2, 128, 512, 800)
+    wl = workload.custom("large_mini_w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
+                         fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
+    run(wl, 3, 3)
+
+
+def test_single_worker():
+    run(bert_mini(W=1, chunk=1024), 3, 3)
+
+
+def test_single_element_and_tiny_tables():
+    for tensors in ([("a", (1,))], [("a", (3,))], [("a", (2,)), ("b", (1,)), ("c", (5,))]):
+        wl = workload.custom("small", tensors, W=2, chunk=256, grad_std=1e-2)
+        run(wl, 2, 2)
+
+
+def test_many_tensors_in_one_chunk():
+    """A chunk that meets more tensors than the per-chunk shared-memory slots
+    (200 tensors of 5 elements), so the per-tensor maximum also takes the
+    global-atomic path."""
+    t = [("big", (3000,))] + [(f"s{i}", (5,)) for i in range(200)] + [("tail", (777,))]
+    wl = workload.custom("many", t, W=4, chunk=2048, grad_std=1e-2)
+    run(wl, 2, 3)
+
+
+def test_odd_worker_count_and_large_w():
+    run(bert_mini(W=37, chunk=512), 1, 2)

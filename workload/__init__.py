@@ -211,6 +211,9 @@ def lib():
         L.wl_gen_grads_f32.argtypes = gen_args
         L.wl_gen_grads_bf16.argtypes = gen_args
         L.wl_gen_params.argtypes = [u64, i64, i64, f32, ctypes.c_void_p]
+        L.wl_gen_grads_range_f32.argtypes = [u64, i64, i32, i64, i64, i32, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             f32, ctypes.c_void_p]
         _lib = L
     return _lib
 
@@ -256,6 +259,24 @@ def gen_grads(wl: Workload, t: int, w: int, N: int | None = None,
     f(wl.seed, t, w, N, wl.L, _ptr(off), _ptr(num), _ptr(std), _ptr(heavy),
       wl.heavy_scale, _ptr(out))
     return out
+
+
+def gen_grads_range(wl: Workload, t: int, w: int, lo: int, hi: int) -> np.ndarray:
+    """Binary32 gradients of worker w at step t for elements [lo, hi) (the
+    bf16 workload's values before rounding to bf16)."""
+    out = np.empty(hi - lo, dtype=np.float32)
+    off, num = wl.offsets, wl.numels
+    std, heavy = wl.layer_std, wl.layer_heavy
+    lib().wl_gen_grads_range_f32(wl.seed, t, w, lo, hi, wl.L, _ptr(off), _ptr(num), _ptr(std),
+                                 _ptr(heavy), wl.heavy_scale, _ptr(out))
+    return out
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Binary32 values rounded to bf16 (nearest even) and widened back."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint32) << 16
+    return r.view(np.float32)
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:

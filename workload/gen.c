@@ -210,3 +210,18 @@ void wl_gen_params(uint64_t seed, int64_t lo, int64_t hi, float std, float* out)
         out[i - lo] = std * z[i & 3];
     }
 }
+
+/* Gradients of worker w at step t for the flat index range [lo, hi) only,
+ * written to out[0 .. hi-lo).  Same values as wl_gen_grads_f32. */
+void wl_gen_grads_range_f32(uint64_t seed, int64_t t, int32_t w, int64_t lo, int64_t hi,
+                            int32_t L, const int64_t* off, const int64_t* numel,
+                            const float* std, const uint8_t* heavy, float heavy_scale,
+                            float* out)
+{
+    int32_t l = 0;
+    for (int64_t i = lo; i < hi; ++i) {
+        while (l < L - 1 && i >= off[l] + numel[l]) ++l;
+        int hv = heavy ? heavy[l] != 0 : 0;
+        out[i - lo] = grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale);
+    }
+}
