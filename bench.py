@@ -45,6 +45,8 @@ def parse_args():
                    choices=("tiny", "base", "large", "large_w32", "gpt2xl"))
     p.add_argument("--max-params", type=int, default=0,
                    help="keep only the leading tensors up to this many parameters (profiling)")
+    p.add_argument("--warmup-stage-steps", type=int, default=-1,
+                   help="LAMB warmup steps before the freeze (default: the workload's)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -326,7 +328,8 @@ def run_ours(args, world, rank, local):
     # warmup stage (LAMB), timed per step for information
     t = 0
     warm_ms, warm_kernel_ms = [], []
-    for _ in range(wl.warmup_steps):
+    n_warm_stage = wl.warmup_steps if args.warmup_stage_steps < 0 else args.warmup_stage_steps
+    for _ in range(n_warm_stage):
         regen(t)
         ev = new_events()
         opt.set_trace_events(ev)
@@ -403,9 +406,10 @@ def run_ours(args, world, rank, local):
                  "ms_p50": float(np.percentile(step_ms, 50)),
                  "ms_p90": float(np.percentile(step_ms, 90)),
                  "worker_elements_per_s": W * value, "wall_s": wall},
-        "warmup_stage": {"ms_per_step": statistics.mean(warm_ms[1:] or warm_ms),
-                         "moments_kernel_ms": statistics.mean(warm_kernel_ms[1:] or warm_kernel_ms),
-                         "params_per_s": N / (statistics.mean(warm_ms[1:] or warm_ms) / 1e3)},
+        "warmup_stage": ({"ms_per_step": statistics.mean(warm_ms[1:] or warm_ms),
+                          "moments_kernel_ms": statistics.mean(warm_kernel_ms[1:] or warm_kernel_ms),
+                          "params_per_s": N / (statistics.mean(warm_ms[1:] or warm_ms) / 1e3),
+                          "steps": len(warm_ms)} if warm_ms else None),
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "e2e": e2e,

@@ -8,232 +8,434 @@
 // worker's sign bits are still live, and the packed words and scales are also
 // written to the exchange buffers (signs_w, scale_w) as the message.
 //
-// Thread map (used by every kernel here): thread `tid` of an NT-thread CTA
-// holds SLOTS aligned float4 groups, group s at chunk offset s*NT*4 + tid*4.
-// Warp w's lanes therefore cover the 128 consecutive elements starting at
-// s*NT*4 + w*128, which is one leaf block of the canonical pairwise tree.
+// Data movement: CTAs are persistent (chunk k = blockIdx.x + i*gridDim.x).
+// Every input tile of a chunk -- the old momentum, each worker's gradient and
+// error, then the server error, frozen and fresh second moments -- is copied
+// into a STAGES-deep ring of shared-memory stages by TMA bulk copies
+// (cp.async.bulk, completion on an mbarrier), issued by thread 0 as soon as a
+// stage is released, so the next tiles stream in while the CTA reduces and
+// stores the current one.  Outputs are written with coalesced 16-byte stores.
+//
+// Thread map: thread `tid` of an NT-thread CTA holds SLOTS aligned float4
+// groups, group s at chunk offset s*NT*4 + tid*4.  Warp w's lanes therefore
+// cover the 128 consecutive elements starting at s*NT*4 + w*128, which is one
+// leaf block of the canonical pairwise tree.
 #include "lamb1b_internal.cuh"
 
 namespace lamb1b {
 
-// Gradients of elements idx..idx+3 of worker w.  Only the first `nv` of them
-// exist (< N); the rest are returned as 0.
-template <int GK>
-__device__ __forceinline__ void grad4(const Grads& G, int w, int64_t idx, int nv,
-                                      const float stdv[4], uint32_t heavy, float g[4])
+// ---- TMA bulk copies and mbarriers (inline PTX, sm_90+) ----------------------
+namespace tma {
+
+__device__ __forceinline__ uint32_t saddr(const void* p)
 {
-    g[0] = g[1] = g[2] = g[3] = 0.0f;
-    if (nv <= 0) return;
-    if constexpr (GK == kGradF32) {
-        const float4 v = *reinterpret_cast<const float4*>(
-            static_cast<const float*>(G.ptr) + (int64_t)w * G.ld + idx);
-        g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
-    } else if constexpr (GK == kGradBF16) {
-        const uint2 v = *reinterpret_cast<const uint2*>(
-            static_cast<const uint16_t*>(G.ptr) + (int64_t)w * G.ld + idx);
-        g[0] = __uint_as_float(v.x << 16);
-        g[1] = __uint_as_float(v.x & 0xFFFF0000u);
-        g[2] = __uint_as_float(v.y << 16);
-        g[3] = __uint_as_float(v.y & 0xFFFF0000u);
-    } else {
-        if (heavy != 0xFu) {
-            float z[4];
-            gen::grads_normal4(G.seed, (uint64_t)idx >> 2, G.t, (uint32_t)w, z);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) g[c] = fmul(stdv[c], z[c]);
-        }
-        if (heavy) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                if ((heavy >> c) & 1u)
-                    g[c] = fmul(G.heavy_scale, gen::student_t3(G.seed, idx + c, G.t, (uint32_t)w));
-        }
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        if (c >= nv) g[c] = 0.0f;
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-template <int NT, int SLOTS, int GK>
-__global__ void __launch_bounds__(NT) k_compress(const Problem P, const Dev D, const Grads G)
+__device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count) : "memory");
+}
+
+// makes the initialised barriers visible to the asynchronous (TMA) proxy
+__device__ __forceinline__ void fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned
+__device__ __forceinline__ void load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(saddr(dst)), "l"(src), "r"(bytes), "r"(saddr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+}  // namespace tma
+
+// Bounded wait for a stage: try_wait suspends for a hardware-defined time per
+// call, so this gives up after seconds, never hangs.
+constexpr uint32_t kMaxWaitTries = 1u << 24;
+
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity)
+{
+    for (uint32_t it = 0; it < kMaxWaitTries; ++it)
+        if (tma::try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Word r of a warp's 128-element block: lanes 8r..8r+7 each hold a nibble of
+// 4 consecutive sign bits; OR-combine them across the 8 lanes.  Every lane of
+// the group returns the word.
+__device__ __forceinline__ uint32_t pack_nibbles(uint32_t nib, int lane)
+{
+    uint32_t v = nib << (4 * (lane & 7));
+    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    return v;
+}
+
+template <int GK>
+struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGradBF16 ? 2 : 0); };
+
+// Per-stage layout: slot A (C floats) then slot B (C floats).  Tiles of one
+// chunk, in order: M (m_old -> A), W worker tiles (g_w -> A, e_w -> B),
+// S (e_s -> A, v -> B), F (v_fresh -> A).
+template <int C>
+struct Ring {
+    static constexpr uint32_t kSlot = C * 4;
+    static constexpr uint32_t kStage = 2 * kSlot;
+};
+
+// Producer side: issue the bulk copies of tile j (chunk i = j / TPC of this
+// CTA, kind r = j % TPC) into stage j % STAGES; called by thread 0 only.
+template <int C, int SG, int STAGES>
+__device__ __forceinline__ void issue_tile(int64_t j, int TPC, const Problem& P, const Dev& D,
+                                        const Grads& G, unsigned char* ring, uint64_t* full)
+{
+    using R = Ring<C>;
+    const int W = P.W;
+    const int64_t i = j / TPC;
+    const int r = (int)(j - i * TPC);
+    const int64_t k = blockIdx.x + i * gridDim.x;
+    const int64_t base = k * C;
+    const int st = (int)(j % STAGES);
+    unsigned char* a = ring + st * R::kStage;
+    unsigned char* b = a + R::kSlot;
+    uint64_t* bar = &full[st];
+    if (r == 0) {
+        tma::arrive_expect_tx(bar, R::kSlot);
+        tma::load(a, D.m + base, R::kSlot, bar);
+    } else if (r <= W) {
+        const int w = r - 1;
+        uint32_t gbytes = 0;
+        if constexpr (SG > 0) {
+            const int64_t n_k = (base + C <= P.N) ? (int64_t)C : P.N - base;
+            gbytes = (uint32_t)(((n_k * SG) + 15) / 16 * 16);
+        }
+        tma::arrive_expect_tx(bar, R::kSlot + gbytes);
+        tma::load(b, D.e_w + (int64_t)w * P.Np + base, R::kSlot, bar);
+        if constexpr (SG > 0)
+            tma::load(a, static_cast<const unsigned char*>(G.ptr) + ((int64_t)w * G.ld + base) * SG,
+                      gbytes, bar);
+    } else if (r == W + 1) {
+        tma::arrive_expect_tx(bar, 2 * R::kSlot);
+        tma::load(a, D.e_s + base, R::kSlot, bar);
+        tma::load(b, D.v + base, R::kSlot, bar);
+    } else {
+        tma::arrive_expect_tx(bar, R::kSlot);
+        tma::load(a, D.v_fresh + base, R::kSlot, bar);
+    }
+}
+
+// Two CTAs per SM when two rings fit in shared memory, else one.
+template <int NT, int SLOTS, int STAGES>
+struct MinBlocks {
+    static constexpr int value = (STAGES * 2 * (NT * 4 * SLOTS) * 4 <= 100 * 1024) ? 2 : 1;
+};
+
+template <int NT, int SLOTS, int GK, int STAGES>
+__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_compress(const Problem P, const Dev D, const Grads G)
 {
     constexpr int NWARP = NT / 32;
     constexpr int C = NT * 4 * SLOTS;
     constexpr int NPART = C / 128;
+    constexpr int SG = GradBytes<GK>::value;
+    using R = Ring<C>;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ uint64_t full[STAGES];
     __shared__ float red[2][NPART];
     __shared__ uint32_t lmax[kMaxChunkLayers];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t k = blockIdx.x;
-    const int64_t base = k * C;
-    const int64_t n_k = (base + C <= P.N) ? (int64_t)C : P.N - base;
-    const float nkf = (float)n_k;
-    const int l0 = D.chunk_l0[k];
+    const int W = P.W;
+    const int TPC = W + 3;                              // tiles per chunk
+    const int64_t nloc = (P.K - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const int64_t total = nloc * TPC;
 
-    for (int i = tid; i < kMaxChunkLayers; i += NT) lmax[i] = 0u;
-
-    int64_t idx[SLOTS];
-    int nv[SLOTS];
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        idx[s] = base + s * NT * 4 + tid * 4;
-        const int64_t r = P.N - idx[s];
-        nv[s] = r >= 4 ? 4 : (r > 0 ? (int)r : 0);
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) tma::bar_init(&full[s], 1);
+        tma::fence_init();
     }
+    for (int i = tid; i < kMaxChunkLayers; i += NT) lmax[i] = 0u;
+    __syncthreads();
 
-    // Per-element gradient std and Student-t flags (in-kernel gradients only).
-    float stdv[SLOTS][4];
-    uint32_t heavy[SLOTS];
-    if constexpr (GK == kGradPhilox) {
-        int l = l0;
-        int64_t lend = D.layer_end[l];
+    // ---- producer (thread 0): tile j goes to stage j % STAGES --------------
+    int64_t issued = 0, released = 0;
+    if (tid == 0)
+        for (; issued < total && issued < STAGES; ++issued)
+            issue_tile<C, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+
+    bool bad = false;        // non-finite gradient seen
+    bool lost = false;       // a stage wait gave up
+
+    for (int64_t ci = 0; ci < nloc; ++ci) {
+        const int64_t k = blockIdx.x + ci * gridDim.x;
+        const int64_t base = k * C;
+        const int64_t n_k = (base + C <= P.N) ? (int64_t)C : P.N - base;
+        const bool full_chunk = n_k == C;
+        const float nkf = (float)n_k;
+        const int64_t j0 = ci * TPC;
+        const int l0 = D.chunk_l0[k];
+
+        int nv[SLOTS];
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
-            heavy[s] = 0u;
+            const int64_t r = P.N - (base + s * NT * 4 + tid * 4);
+            nv[s] = r >= 4 ? 4 : (r > 0 ? (int)r : 0);
+        }
+
+        // in-kernel gradients: per-element std and Student-t flags
+        float stdv[SLOTS][4];
+        uint32_t heavy[SLOTS];
+        if constexpr (GK == kGradPhilox) {
+            int l = l0;
+            int64_t lend = D.layer_end[l];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                stdv[s][c] = 0.0f;
-                if (c < nv[s]) {
-                    while (idx[s] + c >= lend) { ++l; lend = D.layer_end[l]; }
-                    stdv[s][c] = G.layer_std[l];
-                    if (G.layer_heavy && G.layer_heavy[l]) heavy[s] |= 1u << c;
+            for (int s = 0; s < SLOTS; ++s) {
+                heavy[s] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    stdv[s][c] = 0.0f;
+                    if (c < nv[s]) {
+                        const int64_t i = base + s * NT * 4 + tid * 4 + c;
+                        while (i >= lend) { ++l; lend = D.layer_end[l]; }
+                        stdv[s][c] = G.layer_std[l];
+                        if (G.layer_heavy && G.layer_heavy[l]) heavy[s] |= 1u << c;
+                    }
                 }
             }
         }
-    } else {
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            heavy[s] = 0u;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) stdv[s][c] = 0.0f;
-        }
-    }
 
-    // beta1 * m_old, kept for the whole chunk (worker momentum and g~).
-    float bm[SLOTS][4], acc[SLOTS][4];
+        // ---- tile M: beta1 * m_old, kept for the whole chunk ---------------
+        float bm[SLOTS][4], acc[SLOTS][4];
+        {
+            const int st = (int)(j0 % STAGES);
+            if (!wait_stage(&full[st], (uint32_t)((j0 / STAGES) & 1))) lost = true;
+            const float* a = reinterpret_cast<const float*>(ring + st * R::kStage);
 #pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        const float4 mo = *reinterpret_cast<const float4*>(D.m + idx[s]);
-        bm[s][0] = fmul(P.beta1, mo.x); bm[s][1] = fmul(P.beta1, mo.y);
-        bm[s][2] = fmul(P.beta1, mo.z); bm[s][3] = fmul(P.beta1, mo.w);
+            for (int s = 0; s < SLOTS; ++s) {
+                const float4 mo = *reinterpret_cast<const float4*>(a + s * NT * 4 + tid * 4);
+                bm[s][0] = fmul(P.beta1, mo.x); bm[s][1] = fmul(P.beta1, mo.y);
+                bm[s][2] = fmul(P.beta1, mo.z); bm[s][3] = fmul(P.beta1, mo.w);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[s][c] = 0.0f;
-    }
-
-    bool bad = false;
-    // ---- phase 1: every worker compresses its chunk k ----------------------
-    for (int w = 0; w < P.W; ++w) {
-        float z[SLOTS][4];
-        float* ew = D.e_w + (int64_t)w * P.Np;
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            float g[4];
-            grad4<GK>(G, w, idx[s], nv[s], stdv[s], heavy[s], g);
-            const float4 e = *reinterpret_cast<const float4*>(ew + idx[s]);
-            const float ee[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if (P.check_finite && c < nv[s] && !isfinite(g[c])) bad = true;
-                const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
-                z[s][c] = (c < nv[s]) ? fadd(mw, ee[c]) : 0.0f;
+                for (int c = 0; c < 4; ++c) acc[s][c] = 0.0f;
             }
-            const float t = warp_tree128(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1]),
-                                         fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3]));
-            if (lane == 0) red[w & 1][s * NWARP + warp] = t;
+        }
+
+        // ---- phase 1: every worker compresses its chunk k -------------------
+        for (int w = 0; w < W; ++w) {
+            const int64_t j = j0 + 1 + w;
+            const int st = (int)(j % STAGES);
+            if (!wait_stage(&full[st], (uint32_t)((j / STAGES) & 1))) lost = true;
+            const unsigned char* a = ring + st * R::kStage;
+            const float* eb = reinterpret_cast<const float*>(a + R::kSlot);
+            float z[SLOTS][4];
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int off = s * NT * 4 + tid * 4;
+                float g[4];
+                if constexpr (GK == kGradF32) {
+                    const float4 v = *reinterpret_cast<const float4*>(a + off * 4);
+                    g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+                } else if constexpr (GK == kGradBF16) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(a + off * 2);
+                    g[0] = __uint_as_float(v.x << 16);
+                    g[1] = __uint_as_float(v.x & 0xFFFF0000u);
+                    g[2] = __uint_as_float(v.y << 16);
+                    g[3] = __uint_as_float(v.y & 0xFFFF0000u);
+                } else {
+                    g[0] = g[1] = g[2] = g[3] = 0.0f;
+                    if (nv[s] > 0) {
+                        if (heavy[s] != 0xFu) {
+                            float zz[4];
+                            gen::grads_normal4(G.seed, (uint64_t)(base + off) >> 2, G.t, (uint32_t)w, zz);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) g[c] = fmul(stdv[s][c], zz[c]);
+                        }
+                        if (heavy[s]) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                if ((heavy[s] >> c) & 1u)
+                                    g[c] = fmul(G.heavy_scale,
+                                                gen::student_t3(G.seed, base + off + c, G.t, (uint32_t)w));
+                        }
+                    }
+                }
+                const float4 e = *reinterpret_cast<const float4*>(eb + off);
+                const float ee[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool valid = full_chunk || c < nv[s];
+                    if (P.check_finite && valid && !isfinite(g[c])) bad = true;
+                    const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
+                    z[s][c] = valid ? fadd(mw, ee[c]) : 0.0f;
+                }
+                const float t = warp_tree128(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1]),
+                                             fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3]));
+                if (lane == 0) red[w & 1][s * NWARP + warp] = t;
+            }
+            if (__syncthreads_or(lost)) goto abort;
+            released += (w == 0) ? 2 : 1;
+            if (tid == 0)
+                for (; issued < total && issued < released + STAGES; ++issued)
+                    issue_tile<C, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+            const float S = tree_over_partials<NPART>(red[w & 1], lane);
+            const float sc = fsqrt(fdiv(S, nkf));
+            uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
+            float* ew = D.e_w + (int64_t)w * P.Np;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int off = s * NT * 4 + tid * 4;
+                uint32_t nib = 0u;
+                float en[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool valid = full_chunk || c < nv[s];
+                    const bool pos = !(z[s][c] < 0.0f);
+                    const float ss = pos ? sc : -sc;
+                    nib |= (valid && pos) ? (1u << c) : 0u;
+                    en[c] = valid ? fsub(z[s][c], ss) : 0.0f;
+                    acc[s][c] = fadd(acc[s][c], ss);
+                }
+                const uint32_t word = pack_nibbles(nib, lane);
+                if ((lane & 7) == 0)
+                    sw[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
+                *reinterpret_cast<float4*>(ew + base + off) = make_float4(en[0], en[1], en[2], en[3]);
+            }
+            if (tid == 0) D.scale_w[(int64_t)w * P.K + k] = sc;
+        }
+
+        // ---- phases 2 and 3: server average, recompression, scatter ----------
+        {
+            const int64_t jS = j0 + W + 1, jF = j0 + W + 2;
+            const int sS = (int)(jS % STAGES), sF = (int)(jF % STAGES);
+            if (!wait_stage(&full[sS], (uint32_t)((jS / STAGES) & 1))) lost = true;
+            if (!wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
+            const float* es_in = reinterpret_cast<const float*>(ring + sS * R::kStage);
+            const float* v_in = es_in + C;
+            const float* vf_in = reinterpret_cast<const float*>(ring + sF * R::kStage);
+            float y[SLOTS][4], vz[SLOTS][4], vfo[SLOTS][4];
+            const float Wf = (float)W;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int off = s * NT * 4 + tid * 4;
+                const float4 e = *reinterpret_cast<const float4*>(es_in + off);
+                const float4 v = *reinterpret_cast<const float4*>(v_in + off);
+                const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
+                const float ee[4] = {e.x, e.y, e.z, e.w};
+                vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
+                vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool valid = full_chunk || c < nv[s];
+                    y[s][c] = valid ? fadd(fdiv(acc[s][c], Wf), ee[c]) : 0.0f;
+                }
+                const float t = warp_tree128(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1]),
+                                             fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3]));
+                if (lane == 0) red[W & 1][s * NWARP + warp] = t;
+            }
+            if (__syncthreads_or(lost)) goto abort;
+            released += 2;
+            if (tid == 0)
+                for (; issued < total && issued < released + STAGES; ++issued)
+                    issue_tile<C, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+            const float SS = tree_over_partials<NPART>(red[W & 1], lane);
+            const float ss = fsqrt(fdiv(SS, nkf));
+
+            int l = l0;
+            int64_t lend = D.layer_end[l];
+            int lcur = -1;
+            uint32_t runmax = 0u;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int off = s * NT * 4 + tid * 4;
+                uint32_t nib = 0u;
+                float es[4], mn[4], vf[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const bool valid = full_chunk || c < nv[s];
+                    const bool pos = !(y[s][c] < 0.0f);
+                    const float sgn = pos ? ss : -ss;
+                    nib |= (valid && pos) ? (1u << c) : 0u;
+                    es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
+                    mn[c] = valid ? sgn : 0.0f;
+                    // reconstructed gradient and fresh second moment
+                    const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
+                    vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
+                    if (valid) {
+                        float rho = fdiv(fadd(fsqrt(vz[s][c]), P.eps), fadd(fsqrt(vf[c]), P.eps));
+                        if (rho != rho) rho = __int_as_float(0x7F800000);
+                        const int64_t i = base + off + c;
+                        while (i >= lend) { ++l; lend = D.layer_end[l]; }
+                        if (l != lcur) {
+                            if (lcur >= 0) {
+                                if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
+                                else atomicMax(&D.Rmax[lcur], runmax);
+                            }
+                            lcur = l;
+                            runmax = 0u;
+                        }
+                        runmax = max(runmax, __float_as_uint(rho));
+                    }
+                }
+                const uint32_t word = pack_nibbles(nib, lane);
+                if ((lane & 7) == 0)
+                    D.signs_s[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
+                *reinterpret_cast<float4*>(D.e_s + base + off) = make_float4(es[0], es[1], es[2], es[3]);
+                *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
+                *reinterpret_cast<float4*>(D.v_fresh + base + off) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+            }
+            if (lcur >= 0) {
+                if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
+                else atomicMax(&D.Rmax[lcur], runmax);
+            }
+            if (tid == 0) D.scale_s[k] = ss;
         }
         __syncthreads();
-        const float S = tree_over_partials<NPART>(red[w & 1], lane);
-        const float sc = fsqrt(fdiv(S, nkf));
-        uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            bool pos[4];
-            float en[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const bool valid = c < nv[s];
-                pos[c] = valid && !(z[s][c] < 0.0f);
-                en[c] = valid ? (pos[c] ? fsub(z[s][c], sc) : fadd(z[s][c], sc)) : 0.0f;
-                acc[s][c] = fadd(acc[s][c], pos[c] ? sc : -sc);
+        {
+            const int nl = D.chunk_l1[k] - l0 + 1;
+            for (int jj = tid; jj < nl && jj < kMaxChunkLayers; jj += NT) {
+                const uint32_t v = lmax[jj];
+                lmax[jj] = 0u;
+                if (v) atomicMax(&D.Rmax[l0 + jj], v);
             }
-            const uint32_t word = pack_signs128(pos[0], pos[1], pos[2], pos[3], lane);
-            if (lane < 4) sw[(idx[s] - tid * 4 + warp * 128) / 32 + lane] = word;
-            *reinterpret_cast<float4*>(ew + idx[s]) = make_float4(en[0], en[1], en[2], en[3]);
         }
-        if (tid == 0) D.scale_w[(int64_t)w * P.K + k] = sc;
     }
     if (bad) atomicOr(D.flags, 1u);
+    return;
 
-    // ---- phases 2 and 3: server average, recompression, scatter -----------
-    float y[SLOTS][4];
-    const float Wf = (float)P.W;
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        const float4 e = *reinterpret_cast<const float4*>(D.e_s + idx[s]);
-        const float ee[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            y[s][c] = (c < nv[s]) ? fadd(fdiv(acc[s][c], Wf), ee[c]) : 0.0f;
-        const float t = warp_tree128(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1]),
-                                     fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3]));
-        if (lane == 0) red[P.W & 1][s * NWARP + warp] = t;
+abort:
+    // A stage wait gave up (never expected).  Record it, let the copies this
+    // CTA still has in flight land (bounded), then leave.
+    if (tid == 0) {
+        atomicOr(D.flags, 2u);
+        const int64_t first = issued > STAGES ? issued - STAGES : 0;
+        for (int64_t j = first; j < issued; ++j)
+            wait_stage(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
     }
     __syncthreads();
-    const float SS = tree_over_partials<NPART>(red[P.W & 1], lane);
-    const float ss = fsqrt(fdiv(SS, nkf));
-
-    int l = l0;
-    int64_t lend = D.layer_end[l];
-    int lcur = -1;
-    uint32_t runmax = 0u;
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        bool pos[4];
-        float es[4], mn[4], vf[4];
-        const float4 vfr = *reinterpret_cast<const float4*>(D.v_fresh + idx[s]);
-        const float4 vfz = *reinterpret_cast<const float4*>(D.v + idx[s]);
-        const float vf_old[4] = {vfr.x, vfr.y, vfr.z, vfr.w};
-        const float vz[4] = {vfz.x, vfz.y, vfz.z, vfz.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const bool valid = c < nv[s];
-            pos[c] = valid && !(y[s][c] < 0.0f);
-            es[c] = valid ? (pos[c] ? fsub(y[s][c], ss) : fadd(y[s][c], ss)) : 0.0f;
-            mn[c] = valid ? (pos[c] ? ss : -ss) : 0.0f;
-            // reconstructed gradient and fresh second moment
-            const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
-            vf[c] = valid ? fadd(fmul(P.beta2, vf_old[c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
-            if (valid) {
-                float rho = fdiv(fadd(fsqrt(vz[c]), P.eps), fadd(fsqrt(vf[c]), P.eps));
-                if (rho != rho) rho = __int_as_float(0x7F800000);
-                const int64_t i = idx[s] + c;
-                while (i >= lend) { ++l; lend = D.layer_end[l]; }
-                if (l != lcur) {
-                    if (lcur >= 0) {
-                        if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
-                        else atomicMax(&D.Rmax[lcur], runmax);
-                    }
-                    lcur = l;
-                    runmax = 0u;
-                }
-                runmax = max(runmax, __float_as_uint(rho));
-            }
-        }
-        const uint32_t word = pack_signs128(pos[0], pos[1], pos[2], pos[3], lane);
-        if (lane < 4) D.signs_s[(idx[s] - tid * 4 + warp * 128) / 32 + lane] = word;
-        *reinterpret_cast<float4*>(D.e_s + idx[s]) = make_float4(es[0], es[1], es[2], es[3]);
-        *reinterpret_cast<float4*>(D.m + idx[s]) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-        *reinterpret_cast<float4*>(D.v_fresh + idx[s]) = make_float4(vf[0], vf[1], vf[2], vf[3]);
-    }
-    if (lcur >= 0) {
-        if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
-        else atomicMax(&D.Rmax[lcur], runmax);
-    }
-    if (tid == 0) D.scale_s[k] = ss;
-    __syncthreads();
-    const int nl = D.chunk_l1[k] - l0 + 1;
-    for (int j = tid; j < nl && j < kMaxChunkLayers; j += NT)
-        if (lmax[j]) atomicMax(&D.Rmax[l0 + j], lmax[j]);
 }
 
 // Per tensor: soft-thresholded factor from the max ratio, coefficient, and
@@ -255,17 +457,40 @@ __global__ void k_factor(const Problem P, const Dev D)
 
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, cudaStream_t st);
 
-template <int NT, int SLOTS>
-static cudaError_t launch_compress_t(const Problem& P, const Dev& D, const Grads& G,
-                                     cudaStream_t st)
+template <int NT, int SLOTS, int GK, int STAGES>
+static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
-    const dim3 grid((unsigned)P.K);
-    switch (G.kind) {
-    case kGradF32:   k_compress<NT, SLOTS, kGradF32><<<grid, NT, 0, st>>>(P, D, G); break;
-    case kGradBF16:  k_compress<NT, SLOTS, kGradBF16><<<grid, NT, 0, st>>>(P, D, G); break;
-    default:         k_compress<NT, SLOTS, kGradPhilox><<<grid, NT, 0, st>>>(P, D, G); break;
+    constexpr int C = NT * 4 * SLOTS;
+    constexpr size_t smem = (size_t)STAGES * Ring<C>::kStage;
+    auto kern = k_compress<NT, SLOTS, GK, STAGES>;
+    // per-device launch shape, computed once per instantiation
+    static int cached_device = -1;
+    static int grid_cap = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (cached_device != dev) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return e;
+        int per_sm = 0, sms = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem))) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+        grid_cap = (per_sm > 0 ? per_sm : 1) * sms;
+        cached_device = dev;
     }
+    const unsigned grid = (unsigned)(P.K < grid_cap ? P.K : grid_cap);
+    kern<<<grid, NT, smem, st>>>(P, D, G);
     return cudaGetLastError();
+}
+
+template <int NT, int SLOTS, int STAGES>
+static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
+{
+    switch (G.kind) {
+    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES>(P, D, G, st);
+    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES>(P, D, G, st);
+    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES>(P, D, G, st);
+    }
 }
 
 cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
@@ -274,12 +499,12 @@ cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, floa
     cudaError_t e;
     if ((e = trace(ev, 0, st)) != cudaSuccess) return e;
     switch (P.C) {
-    case 256:  e = launch_compress_t<64, 1>(P, D, G, st); break;
-    case 512:  e = launch_compress_t<128, 1>(P, D, G, st); break;
-    case 1024: e = launch_compress_t<256, 1>(P, D, G, st); break;
-    case 2048: e = launch_compress_t<256, 2>(P, D, G, st); break;
-    case 4096: e = launch_compress_t<256, 4>(P, D, G, st); break;
-    case 8192: e = launch_compress_t<512, 4>(P, D, G, st); break;
+    case 256:  e = launch_kind<64, 1, 8>(P, D, G, st); break;
+    case 512:  e = launch_kind<128, 1, 8>(P, D, G, st); break;
+    case 1024: e = launch_kind<256, 1, 8>(P, D, G, st); break;
+    case 2048: e = launch_kind<256, 2, 6>(P, D, G, st); break;
+    case 4096: e = launch_kind<256, 4, 3>(P, D, G, st); break;
+    case 8192: e = launch_kind<512, 4, 3>(P, D, G, st); break;
     default:   return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
