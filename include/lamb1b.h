@@ -214,6 +214,34 @@ int lamb1b_check_status(lamb1b_ctx* ctx, void* stream);
  * Errors: ARG for other n or NULL events with n == 4. */
 int lamb1b_set_trace_events(lamb1b_ctx* ctx, void* const* events, int32_t n);
 
+/* Allocation-free per-tensor sums of squares (the paper has no counterpart;
+ * this is a convenience for callers that cannot allocate device memory).
+ *
+ * out_dev[l] = sum over tensor l of x_i^2, in the same canonical pairwise-tree
+ * order as the warmup step's Sx (lamb1b_state.Sx), for the table `layers`
+ * (host array of L entries, contiguous from 0, as for lamb1b_init).
+ *
+ * Who needs it: code that may not call cudaMalloc/cudaFree or size a
+ * workspace -- a plug-in living inside a framework whose caching allocator
+ * owns all device memory, or a latency-critical loop where cudaMalloc and
+ * cudaFree would synchronise the device.  Such a caller still owns x_dev (N
+ * binary32, 16-byte aligned) and out_dev (L binary32); all scratch comes from
+ * a fixed array inside this library (about 16 MiB, set aside on every GPU that
+ * loads the library until the process exits).  No call allocates.
+ *
+ * Limits: L <= 4096 and at most 2^22 half-granule partial sums (2 per aligned
+ * 256-element granule a tensor meets, so N up to about 5.3e8); larger inputs
+ * return LAMB1B_ERR_ARG without touching the GPU.
+ * The first call on a device looks up the scratch array's device address for
+ * that device (make that first call before any stream capture); later calls
+ * reuse it.  Every call reuses the same scratch, which keeps the previous
+ * call's contents; the call clears what it needs.  Calls that overlap on the
+ * GPU (different streams, or different host threads) race on the scratch:
+ * serialise them.  The host table is staged before the call returns.
+ * Errors: ARG, ALIGN (x_dev), CUDA. */
+int lamb1b_tensor_sumsq_noalloc(const float* x_dev, const lamb1b_layer* layers, int32_t L,
+                                float* out_dev, void* stream);
+
 /* Frees the host context (not the caller's device memory).  NULL is a no-op. */
 int lamb1b_destroy(lamb1b_ctx* ctx);
 
