@@ -1,15 +1,16 @@
 // Compression stage of 1-bit LAMB (arXiv 2104.06069): the fused worker +
 // server pass and the per-tensor factor.
 //
-// One CTA owns one chunk of C elements for all W virtual workers, so the
+// One CTA owns a tile of whole chunks for all W virtual workers, so the
 // "communication" of the compressed allreduce (section 5 summary: gather chunk
 // k of every worker at server k, average, scatter the average) happens in
 // registers: the worker loop accumulates each element's server sum while the
 // worker's sign bits are still live, and the packed words and scales are also
 // written to the exchange buffers (signs_w, scale_w) as the message.
 //
-// Data movement: CTAs are persistent (chunk k = blockIdx.x + i*gridDim.x).
-// Every input tile of a chunk -- the old momentum, each worker's gradient and
+// Data movement: CTAs are persistent (tile t = blockIdx.x + i*gridDim.x; a
+// tile is 4096 elements = 4096/C chunks, or one 8192-element chunk).
+// Every input of a tile -- the old momentum, each worker's gradient and
 // error, then the server error, frozen and fresh second moments -- is copied
 // into a STAGES-deep ring of shared-memory stages by TMA bulk copies
 // (cp.async.bulk, completion on an mbarrier), issued by thread 0 as soon as a
@@ -99,27 +100,28 @@ __device__ __forceinline__ uint32_t pack_nibbles(uint32_t nib, int lane)
 template <int GK>
 struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGradBF16 ? 2 : 0); };
 
-// Per-stage layout: slot A (C floats) then slot B (C floats).  Tiles of one
-// chunk, in order: M (m_old -> A), W worker tiles (g_w -> A, e_w -> B),
-// S (e_s -> A, v -> B), F (v_fresh -> A).
-template <int C>
+// Per-stage layout: slot A (TILE floats) then slot B (TILE floats).  Per tile
+// (TILE consecutive elements = TILE/C whole chunks, or exactly one chunk when
+// C == TILE), the tiles streamed in order are: M (m_old -> A), W worker tiles
+// (g_w -> A, e_w -> B), S (e_s -> A, v -> B), F (v_fresh -> A).
+template <int TILE>
 struct Ring {
-    static constexpr uint32_t kSlot = C * 4;
+    static constexpr uint32_t kSlot = TILE * 4;
     static constexpr uint32_t kStage = 2 * kSlot;
 };
 
-// Producer side: issue the bulk copies of tile j (chunk i = j / TPC of this
-// CTA, kind r = j % TPC) into stage j % STAGES; called by thread 0 only.
-template <int C, int SG, int STAGES>
-__device__ __forceinline__ void issue_tile(int64_t j, int TPC, const Problem& P, const Dev& D,
-                                        const Grads& G, unsigned char* ring, uint64_t* full)
+// Producer side: issue the bulk copies of stream item j (tile i = j / TPC of
+// this CTA, kind r = j % TPC) into stage j % STAGES; called by thread 0 only.
+template <int TILE, int SG, int STAGES>
+__device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P, const Dev& D,
+                                           const Grads& G, unsigned char* ring, uint64_t* full)
 {
-    using R = Ring<C>;
+    using R = Ring<TILE>;
     const int W = P.W;
     const int64_t i = j / TPC;
     const int r = (int)(j - i * TPC);
-    const int64_t k = blockIdx.x + i * gridDim.x;
-    const int64_t base = k * C;
+    const int64_t t = blockIdx.x + i * gridDim.x;
+    const int64_t base = t * TILE;
     const int st = (int)(j % STAGES);
     unsigned char* a = ring + st * R::kStage;
     unsigned char* b = a + R::kSlot;
@@ -131,8 +133,8 @@ __device__ __forceinline__ void issue_tile(int64_t j, int TPC, const Problem& P,
         const int w = r - 1;
         uint32_t gbytes = 0;
         if constexpr (SG > 0) {
-            const int64_t n_k = (base + C <= P.N) ? (int64_t)C : P.N - base;
-            gbytes = (uint32_t)(((n_k * SG) + 15) / 16 * 16);
+            const int64_t n_t = (base + TILE <= P.N) ? (int64_t)TILE : P.N - base;
+            gbytes = (uint32_t)(((n_t * SG) + 15) / 16 * 16);
         }
         tma::arrive_expect_tx(bar, R::kSlot + gbytes);
         tma::load(b, D.e_w + (int64_t)w * P.Np + base, R::kSlot, bar);
@@ -149,20 +151,54 @@ __device__ __forceinline__ void issue_tile(int64_t j, int TPC, const Problem& P,
     }
 }
 
+// Chunk totals from the tile's 128-leaf partials red[0 .. NPART) (element
+// order).  Lane j returns the canonical sum of squares of chunk j / LPC of
+// the tile, LPC = lanes per chunk: the first log2(LPC) butterfly stages are
+// exactly the pairwise tree over each chunk's partials.
+template <int NPART, int PPC>
+__device__ __forceinline__ float chunk_totals(const float* red, int lane)
+{
+    constexpr int PER = NPART > 32 ? NPART / 32 : 1;
+    constexpr int LPC = PPC / PER;
+    static_assert(PPC % PER == 0 && LPC >= 1 && LPC <= 32, "chunk / tile shape");
+    float v;
+    if constexpr (PER == 1) {
+        v = (lane < NPART) ? red[lane] : 0.0f;
+    } else {
+        float t[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) t[j] = red[lane * PER + j];
+#pragma unroll
+        for (int w = 1; w < PER; w <<= 1)
+#pragma unroll
+            for (int j = 0; j < PER; j += 2 * w) t[j] = fadd(t[j], t[j + w]);
+        v = t[0];
+    }
+#pragma unroll
+    for (int o = 1; o < LPC; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
 // Two CTAs per SM when two rings fit in shared memory, else one.
 template <int NT, int SLOTS, int STAGES>
 struct MinBlocks {
     static constexpr int value = (STAGES * 2 * (NT * 4 * SLOTS) * 4 <= 100 * 1024) ? 2 : 1;
 };
 
-template <int NT, int SLOTS, int GK, int STAGES>
-__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_compress(const Problem P, const Dev D, const Grads G)
+template <int NT, int SLOTS, int GK, int STAGES, int C>
+__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
+    k_compress(const Problem P, const Dev D, const Grads G)
 {
     constexpr int NWARP = NT / 32;
-    constexpr int C = NT * 4 * SLOTS;
-    constexpr int NPART = C / 128;
+    constexpr int TILE = NT * 4 * SLOTS;
+    constexpr int NPART = TILE / 128;           // 128-leaf partials per tile
+    constexpr int PPC = C / 128;                // partials per chunk
+    constexpr int PER = NPART > 32 ? NPART / 32 : 1;
+    constexpr int LPC = PPC / PER;              // lanes per chunk in chunk_totals
+    constexpr int CPT = TILE / C;               // chunks per tile
     constexpr int SG = GradBytes<GK>::value;
-    using R = Ring<C>;
+    static_assert(TILE % C == 0, "a tile holds whole chunks");
+    using R = Ring<TILE>;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ uint64_t full[STAGES];
     __shared__ float red[2][NPART];
@@ -170,8 +206,9 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = P.W;
-    const int TPC = W + 3;                              // tiles per chunk
-    const int64_t nloc = (P.K - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const int TPC = W + 3;                              // stream items per tile
+    const int64_t ntiles = P.Np / TILE;
+    const int64_t nloc = (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
     const int64_t total = nloc * TPC;
 
     if (tid == 0) {
@@ -181,29 +218,36 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
     for (int i = tid; i < kMaxChunkLayers; i += NT) lmax[i] = 0u;
     __syncthreads();
 
-    // ---- producer (thread 0): tile j goes to stage j % STAGES --------------
+    // ---- producer (thread 0): item j goes to stage j % STAGES --------------
     int64_t issued = 0, released = 0;
     if (tid == 0)
         for (; issued < total && issued < STAGES; ++issued)
-            issue_tile<C, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+            issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
 
     bool bad = false;        // non-finite gradient seen
     bool lost = false;       // a stage wait gave up
 
-    for (int64_t ci = 0; ci < nloc; ++ci) {
-        const int64_t k = blockIdx.x + ci * gridDim.x;
-        const int64_t base = k * C;
-        const int64_t n_k = (base + C <= P.N) ? (int64_t)C : P.N - base;
-        const bool full_chunk = n_k == C;
-        const float nkf = (float)n_k;
-        const int64_t j0 = ci * TPC;
-        const int l0 = D.chunk_l0[k];
+    for (int64_t ti = 0; ti < nloc; ++ti) {
+        const int64_t tile = blockIdx.x + ti * gridDim.x;
+        const int64_t base = tile * TILE;
+        const bool full_tile = base + TILE <= P.N;
+        const int64_t j0 = ti * TPC;
+        const int64_t k0 = base / C;                     // first chunk of the tile
+        const int64_t klast = (k0 + CPT - 1 < P.K - 1) ? k0 + CPT - 1 : P.K - 1;
+        const int l0 = D.chunk_l0[k0];
+        // this lane's chunk in chunk_totals, and its element count
+        const int64_t kq = k0 + lane / LPC;
+        const int64_t nq_raw = P.N - kq * C;
+        const float nq = (float)(nq_raw >= C ? C : (nq_raw > 0 ? nq_raw : 0));
+        const bool lane_stores_scale = (lane % LPC) == 0 && lane / LPC < CPT && kq < P.K;
 
         int nv[SLOTS];
+        int qsrc[SLOTS];       // lane holding the scale of this slot's chunk
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int64_t r = P.N - (base + s * NT * 4 + tid * 4);
             nv[s] = r >= 4 ? 4 : (r > 0 ? (int)r : 0);
+            qsrc[s] = ((s * NT * 4 + warp * 128) / C) * LPC;
         }
 
         // in-kernel gradients: per-element std and Student-t flags
@@ -228,7 +272,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
             }
         }
 
-        // ---- tile M: beta1 * m_old, kept for the whole chunk ---------------
+        // ---- item M: beta1 * m_old, kept for the whole tile ------------------
         float bm[SLOTS][4], acc[SLOTS][4];
         {
             const int st = (int)(j0 % STAGES);
@@ -244,7 +288,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
             }
         }
 
-        // ---- phase 1: every worker compresses its chunk k -------------------
+        // ---- phase 1: every worker compresses its chunks ----------------------
         for (int w = 0; w < W; ++w) {
             const int64_t j = j0 + 1 + w;
             const int st = (int)(j % STAGES);
@@ -287,7 +331,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
                 const float ee[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_chunk || c < nv[s];
+                    const bool valid = full_tile || c < nv[s];
                     if (P.check_finite && valid && !isfinite(g[c])) bad = true;
                     const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
                     z[s][c] = valid ? fadd(mw, ee[c]) : 0.0f;
@@ -300,19 +344,20 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
             released += (w == 0) ? 2 : 1;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_tile<C, SG, STAGES>(issued, TPC, P, D, G, ring, full);
-            const float S = tree_over_partials<NPART>(red[w & 1], lane);
-            const float sc = fsqrt(fdiv(S, nkf));
+                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+            const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
+            const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
             uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
             float* ew = D.e_w + (int64_t)w * P.Np;
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
                 const int off = s * NT * 4 + tid * 4;
+                const float sc = (CPT == 1) ? sq : __shfl_sync(0xFFFFFFFFu, sq, qsrc[s]);
                 uint32_t nib = 0u;
                 float en[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_chunk || c < nv[s];
+                    const bool valid = full_tile || c < nv[s];
                     const bool pos = !(z[s][c] < 0.0f);
                     const float ss = pos ? sc : -sc;
                     nib |= (valid && pos) ? (1u << c) : 0u;
@@ -324,7 +369,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
                     sw[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
                 *reinterpret_cast<float4*>(ew + base + off) = make_float4(en[0], en[1], en[2], en[3]);
             }
-            if (tid == 0) D.scale_w[(int64_t)w * P.K + k] = sc;
+            if (warp == 0 && lane_stores_scale) D.scale_w[(int64_t)w * P.K + kq] = sq;
         }
 
         // ---- phases 2 and 3: server average, recompression, scatter ----------
@@ -334,7 +379,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
             if (!wait_stage(&full[sS], (uint32_t)((jS / STAGES) & 1))) lost = true;
             if (!wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
             const float* es_in = reinterpret_cast<const float*>(ring + sS * R::kStage);
-            const float* v_in = es_in + C;
+            const float* v_in = es_in + TILE;
             const float* vf_in = reinterpret_cast<const float*>(ring + sF * R::kStage);
             float y[SLOTS][4], vz[SLOTS][4], vfo[SLOTS][4];
             const float Wf = (float)W;
@@ -349,7 +394,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
                 vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_chunk || c < nv[s];
+                    const bool valid = full_tile || c < nv[s];
                     y[s][c] = valid ? fadd(fdiv(acc[s][c], Wf), ee[c]) : 0.0f;
                 }
                 const float t = warp_tree128(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1]),
@@ -360,9 +405,9 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
             released += 2;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_tile<C, SG, STAGES>(issued, TPC, P, D, G, ring, full);
-            const float SS = tree_over_partials<NPART>(red[W & 1], lane);
-            const float ss = fsqrt(fdiv(SS, nkf));
+                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+            const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
+            const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
 
             int l = l0;
             int64_t lend = D.layer_end[l];
@@ -371,11 +416,12 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
                 const int off = s * NT * 4 + tid * 4;
+                const float ss = (CPT == 1) ? ssq : __shfl_sync(0xFFFFFFFFu, ssq, qsrc[s]);
                 uint32_t nib = 0u;
                 float es[4], mn[4], vf[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_chunk || c < nv[s];
+                    const bool valid = full_tile || c < nv[s];
                     const bool pos = !(y[s][c] < 0.0f);
                     const float sgn = pos ? ss : -ss;
                     nib |= (valid && pos) ? (1u << c) : 0u;
@@ -411,11 +457,11 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value)) k_c
                 if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
                 else atomicMax(&D.Rmax[lcur], runmax);
             }
-            if (tid == 0) D.scale_s[k] = ss;
+            if (warp == 0 && lane_stores_scale) D.scale_s[kq] = ssq;
         }
         __syncthreads();
         {
-            const int nl = D.chunk_l1[k] - l0 + 1;
+            const int nl = D.chunk_l1[klast] - l0 + 1;
             for (int jj = tid; jj < nl && jj < kMaxChunkLayers; jj += NT) {
                 const uint32_t v = lmax[jj];
                 lmax[jj] = 0u;
@@ -457,12 +503,12 @@ __global__ void k_factor(const Problem P, const Dev D)
 
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, cudaStream_t st);
 
-template <int NT, int SLOTS, int GK, int STAGES>
+template <int NT, int SLOTS, int GK, int STAGES, int C>
 static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
-    constexpr int C = NT * 4 * SLOTS;
-    constexpr size_t smem = (size_t)STAGES * Ring<C>::kStage;
-    auto kern = k_compress<NT, SLOTS, GK, STAGES>;
+    constexpr int TILE = NT * 4 * SLOTS;
+    constexpr size_t smem = (size_t)STAGES * Ring<TILE>::kStage;
+    auto kern = k_compress<NT, SLOTS, GK, STAGES, C>;
     // per-device launch shape, computed once per instantiation
     static int cached_device = -1;
     static int grid_cap = 0;
@@ -478,19 +524,26 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
         grid_cap = (per_sm > 0 ? per_sm : 1) * sms;
         cached_device = dev;
     }
-    const unsigned grid = (unsigned)(P.K < grid_cap ? P.K : grid_cap);
+    const int64_t ntiles = P.Np / TILE;
+    const unsigned grid = (unsigned)(ntiles < grid_cap ? ntiles : grid_cap);
     kern<<<grid, NT, smem, st>>>(P, D, G);
     return cudaGetLastError();
 }
 
-template <int NT, int SLOTS, int STAGES>
+template <int NT, int SLOTS, int STAGES, int C>
 static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     switch (G.kind) {
-    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES>(P, D, G, st);
-    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES>(P, D, G, st);
-    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES>(P, D, G, st);
+    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES, C>(P, D, G, st);
+    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES, C>(P, D, G, st);
+    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES, C>(P, D, G, st);
     }
+}
+
+int64_t padded_length(int64_t N, int C)
+{
+    const int64_t tile = C > 4096 ? C : 4096;
+    return (N + tile - 1) / tile * tile;
 }
 
 cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
@@ -498,13 +551,15 @@ cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, floa
 {
     cudaError_t e;
     if ((e = trace(ev, 0, st)) != cudaSuccess) return e;
+    // 4096-element tiles (256 threads x 4 float4 groups) holding 4096/C chunks;
+    // 8192-element chunks use 512-thread tiles of one chunk.
     switch (P.C) {
-    case 256:  e = launch_kind<64, 1, 8>(P, D, G, st); break;
-    case 512:  e = launch_kind<128, 1, 8>(P, D, G, st); break;
-    case 1024: e = launch_kind<256, 1, 8>(P, D, G, st); break;
-    case 2048: e = launch_kind<256, 2, 6>(P, D, G, st); break;
-    case 4096: e = launch_kind<256, 4, 3>(P, D, G, st); break;
-    case 8192: e = launch_kind<512, 4, 3>(P, D, G, st); break;
+    case 256:  e = launch_kind<256, 4, 3, 256>(P, D, G, st); break;
+    case 512:  e = launch_kind<256, 4, 3, 512>(P, D, G, st); break;
+    case 1024: e = launch_kind<256, 4, 3, 1024>(P, D, G, st); break;
+    case 2048: e = launch_kind<256, 4, 3, 2048>(P, D, G, st); break;
+    case 4096: e = launch_kind<256, 4, 3, 4096>(P, D, G, st); break;
+    case 8192: e = launch_kind<512, 4, 3, 8192>(P, D, G, st); break;
     default:   return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

@@ -74,7 +74,7 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     p->C = hp->chunk;
     p->K = (N + p->C - 1) / p->C;
     if (p->K > 0x7FFFFFFFll) return LAMB1B_ERR_ARG;
-    p->Np = p->K * p->C;
+    p->Np = lamb1b::padded_length(N, p->C);   // whole compression tiles
     p->words_ld = p->Np / 32;
     p->H = H;
     const size_t f = sizeof(float);

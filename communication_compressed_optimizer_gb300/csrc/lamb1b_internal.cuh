@@ -15,7 +15,7 @@ constexpr int kMaxChunkLayers = 64;  // per-chunk layer slots kept in shared mem
 
 struct Problem {
     int64_t N;        // parameters
-    int64_t Np;       // K * C, padded vector length
+    int64_t Np;       // padded vector length: a multiple of max(C, 4096) >= K * C
     int64_t K;        // chunks
     int64_t words_ld; // Np / 32
     int32_t L, W, C;
@@ -156,5 +156,7 @@ inline cudaError_t trace(const cudaEvent_t* ev, int i, cudaStream_t st)
     return ev ? cudaEventRecord(ev[i], st) : cudaSuccess;
 }
 cudaError_t launch_init_layers(const Problem& P, const Dev& D, cudaStream_t st);
+// padded vector length for N elements and chunk C (whole compression tiles)
+int64_t padded_length(int64_t N, int C);
 
 }  // namespace lamb1b

@@ -111,7 +111,8 @@ typedef struct {
 
 /* Device views of the optimizer state inside the workspace (for inspection,
  * checkpointing and restore; the caller may read or overwrite them between
- * calls).  Padded layouts: Np = K*C elements per vector, words_ld = Np/32.
+ * calls).  Padded layouts: Np = N rounded up to a multiple of max(C, 4096)
+ * elements per vector (>= K*C), words_ld = Np/32.
  *   m, v, v_fresh, e_s: [Np] binary32; elements >= N are kept at 0
  *   e_w: [W][Np];   signs_w: [W][words_ld] u32;   signs_s: [words_ld]
  *   scale_w: [W][K];   scale_s: [K]
