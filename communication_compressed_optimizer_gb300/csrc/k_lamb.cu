@@ -22,7 +22,10 @@ __device__ __forceinline__ int first_layer_of_block(const Problem& P, const Dev&
 // ---- update: x = x - (lr c_l) (m / (sqrt(v) + eps) + wd x) ----------------
 // Warmup: m, v are this step's moments.  Compression stage: m is the
 // decompressed server momentum and v the frozen second moment.
-__global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, float* __restrict__ x)
+// msig: m is the decompressed server momentum of this step, read from its sign
+// words and chunk scales (1/32 of the bytes) instead of the dense copy.
+__global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, float* __restrict__ x,
+                                                int msig)
 {
     const int tid = threadIdx.x;
     const int64_t b0 = (int64_t)blockIdx.x * kBlock;
@@ -33,9 +36,17 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
     for (int s = 0; s < kSlots; ++s) {
         const int64_t idx = b0 + s * kNT * 4 + tid * 4;
         if (idx >= P.N) break;
-        const float4 m4 = *reinterpret_cast<const float4*>(D.m + idx);
+        float mm[4];
+        if (msig) {
+            const uint32_t word = D.signs_s[idx / 32];
+            const float sc = D.scale_s[idx / P.C];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) mm[c] = ((word >> ((idx & 31) + c)) & 1u) ? sc : -sc;
+        } else {
+            const float4 m4 = *reinterpret_cast<const float4*>(D.m + idx);
+            mm[0] = m4.x; mm[1] = m4.y; mm[2] = m4.z; mm[3] = m4.w;
+        }
         const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
         const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
         const bool full = idx + 4 <= P.N;
         float xv[4];
@@ -65,10 +76,10 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
     }
 }
 
-cudaError_t launch_update(const Problem& P, const Dev& D, float* x, cudaStream_t st)
+cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st)
 {
     const unsigned grid = (unsigned)((P.N + kBlock - 1) / kBlock);
-    k_update<<<grid, kNT, 0, st>>>(P, D, x);
+    k_update<<<grid, kNT, 0, st>>>(P, D, x, msig);
     return cudaGetLastError();
 }
 
@@ -278,7 +289,7 @@ cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float*
     k_layer_finish<<<(unsigned)P.L, kNT, 0, st>>>(P, D, first_warmup);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = trace(ev, 2, st)) != cudaSuccess) return e;
-    if ((e = launch_update(P, D, x, st)) != cudaSuccess) return e;
+    if ((e = launch_update(P, D, x, 0, st)) != cudaSuccess) return e;
     return trace(ev, 3, st);
 }
 
