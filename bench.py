@@ -74,15 +74,13 @@ def grad_bytes(wl):
 
 
 def fused_kernel_bytes(wl):
-    """Algorithmic HBM bytes of one launch of the fused compression kernel in
-    steady state (every compression step after the first): per parameter
-    W*(g + 4 e_w + 4 e_w + 1/8 signs) + reads 1/8 (previous server signs, in
-    place of m) + 4 e_s + 4 v + 4 v_fresh and writes 4 e_s + 4 m + 4 v_fresh +
-    1/8 server signs; plus 4 bytes per scale (W worker + 1 server written,
-    1 previous server scale read)."""
+    """Algorithmic HBM bytes of one launch of the fused compression kernel:
+    per parameter W*(g + 4 e_w read + 4 e_w written + 1/8 signs) + reads of
+    4 m + 4 e_s + 4 v + 4 v_fresh and writes of 4 e_s + 4 m + 4 v_fresh +
+    1/8 server signs; plus 4 bytes per written scale (W worker + 1 server)."""
     W = wl.W
-    per = W * (grad_bytes(wl) + 8.125) + 24.25
-    return wl.N * per + 4.0 * wl.K * (W + 2)
+    per = W * (grad_bytes(wl) + 8.125) + 28.125
+    return wl.N * per + 4.0 * wl.K * (W + 1)
 
 
 def update_kernel_bytes(wl):

@@ -102,8 +102,7 @@ struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGra
 
 // Per-stage layout: slot A (TILE floats) then slot B (TILE floats).  Per tile
 // (TILE consecutive elements = TILE/C whole chunks, or exactly one chunk when
-// C == TILE), the tiles streamed in order are: M (m_old, or after the first
-// compression step the previous server sign words, -> A), W worker tiles
+// C == TILE), the tiles streamed in order are: M (m_old -> A), W worker tiles
 // (g_w -> A, e_w -> B), S (e_s -> A, v -> B), F (v_fresh -> A).
 template <int TILE>
 struct Ring {
@@ -115,8 +114,7 @@ struct Ring {
 // this CTA, kind r = j % TPC) into stage j % STAGES; called by thread 0 only.
 template <int TILE, int SG, int STAGES>
 __device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P, const Dev& D,
-                                           const Grads& G, unsigned char* ring, uint64_t* full,
-                                           int msig)
+                                           const Grads& G, unsigned char* ring, uint64_t* full)
 {
     using R = Ring<TILE>;
     const int W = P.W;
@@ -129,13 +127,8 @@ __device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P,
     unsigned char* b = a + R::kSlot;
     uint64_t* bar = &full[st];
     if (r == 0) {
-        if (msig) {   // the previous step's server sign words of this tile
-            tma::arrive_expect_tx(bar, TILE / 8);
-            tma::load(a, D.signs_s + base / 32, TILE / 8, bar);
-        } else {
-            tma::arrive_expect_tx(bar, R::kSlot);
-            tma::load(a, D.m + base, R::kSlot, bar);
-        }
+        tma::arrive_expect_tx(bar, R::kSlot);
+        tma::load(a, D.m + base, R::kSlot, bar);
     } else if (r <= W) {
         const int w = r - 1;
         uint32_t gbytes = 0;
@@ -194,7 +187,7 @@ struct MinBlocks {
 
 template <int NT, int SLOTS, int GK, int STAGES, int C>
 __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
-    k_compress(const Problem P, const Dev D, const Grads G, int msig)
+    k_compress(const Problem P, const Dev D, const Grads G)
 {
     constexpr int NWARP = NT / 32;
     constexpr int TILE = NT * 4 * SLOTS;
@@ -229,7 +222,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
     int64_t issued = 0, released = 0;
     if (tid == 0)
         for (; issued < total && issued < STAGES; ++issued)
-            issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full, msig);
+            issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
 
     bool bad = false;        // non-finite gradient seen
     bool lost = false;       // a stage wait gave up
@@ -287,27 +280,11 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             const float* a = reinterpret_cast<const float*>(ring + st * R::kStage);
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                float mo[4];
-                if (msig) {
-                    // m_old is exactly last step's server sign x server scale
-                    const uint32_t word = reinterpret_cast<const uint32_t*>(a)[off / 32];
-                    const int64_t kprev = k0 + (s * NT * 4 + warp * 128) / C;
-                    const float sprev = kprev < P.K ? D.scale_s[kprev] : 0.0f;
+                const float4 mo = *reinterpret_cast<const float4*>(a + s * NT * 4 + tid * 4);
+                bm[s][0] = fmul(P.beta1, mo.x); bm[s][1] = fmul(P.beta1, mo.y);
+                bm[s][2] = fmul(P.beta1, mo.z); bm[s][3] = fmul(P.beta1, mo.w);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const bool valid = full_tile || c < nv[s];
-                        mo[c] = valid ? (((word >> ((off & 31) + c)) & 1u) ? sprev : -sprev) : 0.0f;
-                    }
-                } else {
-                    const float4 v = *reinterpret_cast<const float4*>(a + off);
-                    mo[0] = v.x; mo[1] = v.y; mo[2] = v.z; mo[3] = v.w;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    bm[s][c] = fmul(P.beta1, mo[c]);
-                    acc[s][c] = 0.0f;
-                }
+                for (int c = 0; c < 4; ++c) acc[s][c] = 0.0f;
             }
         }
 
@@ -367,7 +344,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             released += (w == 0) ? 2 : 1;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full, msig);
+                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
             const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
             const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
             uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
@@ -428,7 +405,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             released += 2;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full, msig);
+                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
             const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
 
@@ -527,8 +504,7 @@ __global__ void k_factor(const Problem P, const Dev D)
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st);
 
 template <int NT, int SLOTS, int GK, int STAGES, int C>
-static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, int msig,
-                              cudaStream_t st)
+static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     constexpr int TILE = NT * 4 * SLOTS;
     constexpr size_t smem = (size_t)STAGES * Ring<TILE>::kStage;
@@ -550,18 +526,17 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, in
     }
     const int64_t ntiles = P.Np / TILE;
     const unsigned grid = (unsigned)(ntiles < grid_cap ? ntiles : grid_cap);
-    kern<<<grid, NT, smem, st>>>(P, D, G, msig);
+    kern<<<grid, NT, smem, st>>>(P, D, G);
     return cudaGetLastError();
 }
 
 template <int NT, int SLOTS, int STAGES, int C>
-static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, int msig,
-                               cudaStream_t st)
+static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     switch (G.kind) {
-    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES, C>(P, D, G, msig, st);
-    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES, C>(P, D, G, msig, st);
-    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES, C>(P, D, G, msig, st);
+    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES, C>(P, D, G, st);
+    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES, C>(P, D, G, st);
+    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES, C>(P, D, G, st);
     }
 }
 
@@ -572,20 +547,19 @@ int64_t padded_length(int64_t N, int C)
 }
 
 cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
-                            cudaStream_t st, const cudaEvent_t* ev, bool m_from_signs)
+                            cudaStream_t st, const cudaEvent_t* ev)
 {
-    const int msig = m_from_signs ? 1 : 0;
     cudaError_t e;
     if ((e = trace(ev, 0, st)) != cudaSuccess) return e;
     // 4096-element tiles (256 threads x 4 float4 groups) holding 4096/C chunks;
     // 8192-element chunks use 512-thread tiles of one chunk.
     switch (P.C) {
-    case 256:  e = launch_kind<256, 4, 3, 256>(P, D, G, msig, st); break;
-    case 512:  e = launch_kind<256, 4, 3, 512>(P, D, G, msig, st); break;
-    case 1024: e = launch_kind<256, 4, 3, 1024>(P, D, G, msig, st); break;
-    case 2048: e = launch_kind<256, 4, 3, 2048>(P, D, G, msig, st); break;
-    case 4096: e = launch_kind<256, 4, 3, 4096>(P, D, G, msig, st); break;
-    case 8192: e = launch_kind<512, 4, 3, 8192>(P, D, G, msig, st); break;
+    case 256:  e = launch_kind<256, 4, 3, 256>(P, D, G, st); break;
+    case 512:  e = launch_kind<256, 4, 3, 512>(P, D, G, st); break;
+    case 1024: e = launch_kind<256, 4, 3, 1024>(P, D, G, st); break;
+    case 2048: e = launch_kind<256, 4, 3, 2048>(P, D, G, st); break;
+    case 4096: e = launch_kind<256, 4, 3, 4096>(P, D, G, st); break;
+    case 8192: e = launch_kind<512, 4, 3, 8192>(P, D, G, st); break;
     default:   return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
@@ -593,7 +567,8 @@ cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, floa
     k_factor<<<(P.L + 255) / 256, 256, 0, st>>>(P, D);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = trace(ev, 2, st)) != cudaSuccess) return e;
-    // the update reads this step's server signs and scales instead of m
+    // the update reads this step's server sign words and chunk scales (m is
+    // exactly server sign x server scale) instead of the dense m
     if ((e = launch_update(P, D, x, 1, st)) != cudaSuccess) return e;
     return trace(ev, 3, st);
 }

@@ -84,7 +84,7 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     bytes[R_SW] = sizeof(uint32_t) * p->words_ld * p->W;
     bytes[R_SS] = sizeof(uint32_t) * p->words_ld;
     bytes[R_SCW] = f * p->K * p->W;
-    bytes[R_SCS] = f * p->K;
+    bytes[R_SCS] = f * (p->K + 16);   // + room for 16-byte aligned windows
     for (int r = R_CBAR; r <= R_RMAX; ++r) bytes[r] = f * L;
     bytes[R_LOFF] = bytes[R_LEND] = sizeof(int64_t) * L;
     bytes[R_HBASE] = sizeof(int64_t) * (L + 1);
@@ -114,7 +114,6 @@ struct lamb1b_ctx {
     int32_t stage = 0;
     std::vector<int64_t> off, end, hbase;
     std::vector<int32_t> l0, l1;
-    bool signs_valid = false;   // signs_s/scale_s hold the last compression step's m
     bool tracing = false;
     cudaEvent_t ev[4] = {};
 };
@@ -320,7 +319,6 @@ extern "C" int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream)
     if (lamb1b::launch_freeze(ctx->P, ctx->D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
     ctx->stage = 1;
-    ctx->signs_valid = false;
     return LAMB1B_OK;
 }
 
@@ -333,9 +331,8 @@ extern "C" int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, 
     if ((rc = grads_check(ctx, grads))) return rc;
     const Grads G = to_grads(ctx, grads);
     if (lamb1b::launch_compress(ctx->P, ctx->D, G, ctx->x, static_cast<cudaStream_t>(stream),
-                                ctx->tracing ? ctx->ev : nullptr, ctx->signs_valid) != cudaSuccess)
+                                ctx->tracing ? ctx->ev : nullptr) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
-    ctx->signs_valid = true;
     ctx->t += 1;
     return LAMB1B_OK;
 }
@@ -364,7 +361,6 @@ extern "C" int lamb1b_set_counters(lamb1b_ctx* ctx, int64_t t, int32_t n_warmup,
     ctx->t = t;
     ctx->n_warm = n_warmup;
     ctx->stage = stage;
-    ctx->signs_valid = false;   // the next step reads the restored dense m
     return LAMB1B_OK;
 }
 

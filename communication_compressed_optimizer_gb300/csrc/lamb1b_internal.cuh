@@ -148,11 +148,8 @@ __device__ __forceinline__ uint32_t pack_signs128(bool p0, bool p1, bool p2, boo
 cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float* x,
                           cudaStream_t st, int first_warmup, const cudaEvent_t* ev);
 cudaError_t launch_freeze(const Problem& P, const Dev& D, cudaStream_t st);
-// m_from_signs: the previous compression step's server words and scales are
-// valid (m == server sign x server scale), so the old momentum is read from
-// them; otherwise from the dense m.
 cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
-                            cudaStream_t st, const cudaEvent_t* ev, bool m_from_signs);
+                            cudaStream_t st, const cudaEvent_t* ev);
 
 inline cudaError_t trace(const cudaEvent_t* ev, int i, cudaStream_t st)
 {
