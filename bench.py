@@ -198,6 +198,14 @@ def barrier(world):
         dist.barrier()
 
 
+def aggregate_throughput(local_seconds, units_per_rank, world):
+    """Whole-job throughput of `world` replicas that each processed
+    units_per_rank units in local_seconds: all units over the slowest rank's
+    time (weak scaling).  Returns (units/s, slowest seconds)."""
+    slowest = max_over_ranks(local_seconds, world)
+    return world * units_per_rank / slowest, slowest
+
+
 def max_over_ranks(value, world):
     if world == 1:
         return value
@@ -372,9 +380,8 @@ def run_ours(args, world, rank, local):
     kern_ms = [e[0].elapsed_time(e[1]) for e in events]
     factor_ms = [e[1].elapsed_time(e[2]) for e in events]
     upd_ms = [e[2].elapsed_time(e[3]) for e in events]
-    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    value, total_s = aggregate_throughput(sum(step_ms) / 1e3, N * args.steps, world)
     ms_per_step = 1e3 * total_s / args.steps
-    value = world * N * args.steps / total_s
 
     peak, peak_kind = measured_peaks()
     kb = fused_kernel_bytes(wl)
