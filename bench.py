@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="large",
                    choices=("tiny", "base", "large", "large_w32", "gpt2xl"))
+    p.add_argument("--variant", choices=("lamb", "adam"), default="lamb",
+                   help="1-bit LAMB (default) or the 1-bit Adam variant")
     p.add_argument("--max-params", type=int, default=0,
                    help="keep only the leading tensors up to this many parameters (profiling)")
     p.add_argument("--warmup-stage-steps", type=int, default=-1,
@@ -73,13 +75,14 @@ def grad_bytes(wl):
     return {"f32": 4, "bf16": 2, "philox": 0}[wl.grad]
 
 
-def fused_kernel_bytes(wl):
+def fused_kernel_bytes(wl, variant="lamb"):
     """Algorithmic HBM bytes of one launch of the fused compression kernel:
     per parameter W*(g + 4 e_w read + 4 e_w written + 1/8 signs) + reads of
     4 m + 4 e_s + 4 v + 4 v_fresh and writes of 4 e_s + 4 m + 4 v_fresh +
     1/8 server signs; plus 4 bytes per written scale (W worker + 1 server)."""
     W = wl.W
-    per = W * (grad_bytes(wl) + 8.125) + 28.125
+    # 1-bit Adam reads and writes no second moments in this kernel
+    per = W * (grad_bytes(wl) + 8.125) + (16.125 if variant == "adam" else 28.125)
     return wl.N * per + 4.0 * wl.K * (W + 1)
 
 
@@ -88,8 +91,8 @@ def update_kernel_bytes(wl):
     return wl.N * 12.125 + 4.0 * wl.K
 
 
-def step_bytes(wl):
-    return fused_kernel_bytes(wl) + update_kernel_bytes(wl)
+def step_bytes(wl, variant="lamb"):
+    return fused_kernel_bytes(wl, variant) + update_kernel_bytes(wl)
 
 
 def measured_peaks():
@@ -319,7 +322,7 @@ def run_ours(args, world, rank, local):
 
     x = torch.empty(N, device="cuda")
     pkg.gen_params(x, 0, N, wl.param_std, wl.seed)
-    opt = pkg.OneBitLamb(x, layers, W, C, **wl.hp)
+    opt = pkg.OneBitLamb(x, layers, W, C, **dict(wl.hp, variant=args.variant))
     if wl.grad == "philox":
         g = pkg.PhiloxGrads(wl.seed, wl.layer_std, wl.layer_heavy, wl.heavy_scale)
 
@@ -384,7 +387,7 @@ def run_ours(args, world, rank, local):
     ms_per_step = 1e3 * total_s / args.steps
 
     peak, peak_kind = measured_peaks()
-    kb = fused_kernel_bytes(wl)
+    kb = fused_kernel_bytes(wl, args.variant)
     k_avg = statistics.mean(kern_ms)
     achieved = kb / (k_avg / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
@@ -401,17 +404,18 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": wl.name, "W": W, "chunk": C, "params": N, "tensors": wl.L,
-                   "grads": wl.grad, "parallelism": f"replicas{world}",
+                   "grads": wl.grad, "variant": f"1-bit {args.variant.upper() if args.variant == 'lamb' else 'Adam'}",
+                   "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each step moves %.1f GB); gradients regenerated "
-                         "on the device between timed steps" % (step_bytes(wl) / 1e9),
+                         "on the device between timed steps" % (step_bytes(wl, args.variant) / 1e9),
                    "timing": "CUDA events on the launching stream around each step"},
         "roofline": {"bound": "hbm", "kernel": "k_compress (fused worker+server pass)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "traffic": traffic, "alg_bytes_per_launch": kb,
                      "kernel_ms": k_avg},
-        "step": {"alg_bytes": step_bytes(wl), "hbm_gbs": step_bytes(wl) / (ms_per_step / 1e3) / 1e9,
-                 "frac_of_peak": step_bytes(wl) / (ms_per_step / 1e3) / 1e9 / peak,
+        "step": {"alg_bytes": step_bytes(wl, args.variant), "hbm_gbs": step_bytes(wl, args.variant) / (ms_per_step / 1e3) / 1e9,
+                 "frac_of_peak": step_bytes(wl, args.variant) / (ms_per_step / 1e3) / 1e9 / peak,
                  "kernel_ms": {"compress": k_avg, "factor": statistics.mean(factor_ms),
                                "update": statistics.mean(upd_ms)},
                  "ms_p10": float(np.percentile(step_ms, 10)),

@@ -45,6 +45,7 @@ def _hparams(W, chunk, hp):
               "coeff_ema", "factor_min", "factor_max", "factor_threshold"):
         setattr(h, k, float(hp[k]))
     h.check_finite = int(hp.get("check_finite", 0))
+    h.variant = {"lamb": 0, "adam": 1}.get(hp.get("variant", 0), hp.get("variant", 0))
     return h
 
 

@@ -142,9 +142,14 @@ __device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P,
             tma::load(a, static_cast<const unsigned char*>(G.ptr) + ((int64_t)w * G.ld + base) * SG,
                       gbytes, bar);
     } else if (r == W + 1) {
-        tma::arrive_expect_tx(bar, 2 * R::kSlot);
-        tma::load(a, D.e_s + base, R::kSlot, bar);
-        tma::load(b, D.v + base, R::kSlot, bar);
+        if (P.adam) {   // 1-bit Adam needs no second moment here
+            tma::arrive_expect_tx(bar, R::kSlot);
+            tma::load(a, D.e_s + base, R::kSlot, bar);
+        } else {
+            tma::arrive_expect_tx(bar, 2 * R::kSlot);
+            tma::load(a, D.e_s + base, R::kSlot, bar);
+            tma::load(b, D.v + base, R::kSlot, bar);
+        }
     } else {
         tma::arrive_expect_tx(bar, R::kSlot);
         tma::load(a, D.v_fresh + base, R::kSlot, bar);
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = P.W;
-    const int TPC = W + 3;                              // stream items per tile
+    const int TPC = W + (P.adam ? 2 : 3);               // stream items per tile
     const int64_t ntiles = P.Np / TILE;
     const int64_t nloc = (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
     const int64_t total = nloc * TPC;
@@ -377,7 +382,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             const int64_t jS = j0 + W + 1, jF = j0 + W + 2;
             const int sS = (int)(jS % STAGES), sF = (int)(jF % STAGES);
             if (!wait_stage(&full[sS], (uint32_t)((jS / STAGES) & 1))) lost = true;
-            if (!wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
+            if (!P.adam && !wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
             const float* es_in = reinterpret_cast<const float*>(ring + sS * R::kStage);
             const float* v_in = es_in + TILE;
             const float* vf_in = reinterpret_cast<const float*>(ring + sF * R::kStage);
@@ -387,11 +392,13 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             for (int s = 0; s < SLOTS; ++s) {
                 const int off = s * NT * 4 + tid * 4;
                 const float4 e = *reinterpret_cast<const float4*>(es_in + off);
-                const float4 v = *reinterpret_cast<const float4*>(v_in + off);
-                const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
                 const float ee[4] = {e.x, e.y, e.z, e.w};
-                vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
-                vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
+                if (!P.adam) {
+                    const float4 v = *reinterpret_cast<const float4*>(v_in + off);
+                    const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
+                    vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
+                    vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
+                }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const bool valid = full_tile || c < nv[s];
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                 if (lane == 0) red[W & 1][s * NWARP + warp] = t;
             }
             if (__syncthreads_or(lost)) goto abort;
-            released += 2;
+            released += P.adam ? 1 : 2;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
                     issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
@@ -427,6 +434,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                     nib |= (valid && pos) ? (1u << c) : 0u;
                     es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
                     mn[c] = valid ? sgn : 0.0f;
+                    if (P.adam) continue;
                     // reconstructed gradient and fresh second moment
                     const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
                     vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
@@ -451,7 +459,9 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                     D.signs_s[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
                 *reinterpret_cast<float4*>(D.e_s + base + off) = make_float4(es[0], es[1], es[2], es[3]);
                 *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-                *reinterpret_cast<float4*>(D.v_fresh + base + off) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+                if (!P.adam)
+                    *reinterpret_cast<float4*>(D.v_fresh + base + off) =
+                        make_float4(vf[0], vf[1], vf[2], vf[3]);
             }
             if (lcur >= 0) {
                 if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
@@ -564,8 +574,10 @@ cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, floa
     }
     if (e != cudaSuccess) return e;
     if ((e = trace(ev, 1, st)) != cudaSuccess) return e;
-    k_factor<<<(P.L + 255) / 256, 256, 0, st>>>(P, D);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!P.adam) {   // 1-bit Adam: c = 1, gc = lr from the initialisation
+        k_factor<<<(P.L + 255) / 256, 256, 0, st>>>(P, D);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if ((e = trace(ev, 2, st)) != cudaSuccess) return e;
     // the update reads this step's server sign words and chunk scales (m is
     // exactly server sign x server scale) instead of the dense m

@@ -187,6 +187,7 @@ __global__ void __launch_bounds__(kNT) k_warmup_moments(const Problem P, const D
             *reinterpret_cast<float4*>(D.m + idx) = make_float4(mm[0], mm[1], mm[2], mm[3]);
             *reinterpret_cast<float4*>(D.v + idx) = make_float4(vv[0], vv[1], vv[2], vv[3]);
         }
+        if (P.adam) continue;   // Adam: no per-tensor norms
         // half-granule partial sums, one per layer meeting this 128-block
         int lo = 0x7FFFFFFF, hi = -1;
 #pragma unroll
@@ -286,8 +287,10 @@ cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float*
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = trace(ev, 1, st)) != cudaSuccess) return e;
-    k_layer_finish<<<(unsigned)P.L, kNT, 0, st>>>(P, D, first_warmup);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!P.adam) {   // Adam keeps c = 1 (gc = lr from the initialisation)
+        k_layer_finish<<<(unsigned)P.L, kNT, 0, st>>>(P, D, first_warmup);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if ((e = trace(ev, 2, st)) != cudaSuccess) return e;
     if ((e = launch_update(P, D, x, 0, st)) != cudaSuccess) return e;
     return trace(ev, 3, st);

@@ -51,6 +51,7 @@ int check_hparams(const lamb1b_hparams* hp)
     if (!(hp->factor_min >= 0.0f && hp->factor_min <= hp->factor_max)) return LAMB1B_ERR_ARG;
     if (!(hp->factor_threshold >= 0.0f)) return LAMB1B_ERR_ARG;
     if (hp->check_finite != 0 && hp->check_finite != 1) return LAMB1B_ERR_ARG;
+    if (hp->variant != 0 && hp->variant != 1) return LAMB1B_ERR_ARG;
     return LAMB1B_OK;
 }
 
@@ -217,6 +218,7 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     P.fthr_hi = 1.0f + hp->factor_threshold;
     P.inv_dummy = 0.0f;
     P.check_finite = hp->check_finite;
+    P.adam = hp->variant == 1 ? 1 : 0;
 
     char* ws = static_cast<char*>(workspace_dev);
     Dev& D = c->D;

@@ -25,6 +25,7 @@ struct Problem {
     float fmin, fmax, fthr_lo, fthr_hi; // fl(1 - thr), fl(1 + thr)
     float inv_dummy;
     int32_t check_finite;
+    int32_t adam;       // 1-bit Adam variant: no layerwise coefficient, no fresh variance
 };
 
 // Device pointers into the caller's workspace.

@@ -80,6 +80,12 @@ typedef struct {
     float factor_threshold;   /* soft threshold: factor moves at most this
                                  fraction of its previous value per step         */
     int32_t check_finite;     /* 1: flag NaN/Inf gradients (lamb1b_check_status) */
+    int32_t variant;          /* 0: 1-bit LAMB.  1: 1-bit Adam (the predecessor
+                                 method in the 1-bit LAMB background): Adam in the
+                                 warmup, the same compressed momentum exchange in
+                                 the compression stage, no layerwise coefficient
+                                 (c = 1), no fresh variance; coeff_* and factor_*
+                                 are then unused. */
 } lamb1b_hparams;
 
 typedef enum {

@@ -43,7 +43,7 @@ _P = ctypes.c_void_p
 class _OrcT(ctypes.Structure):
     _fields_ = [
         ("N", ctypes.c_int64), ("L", ctypes.c_int32), ("W", ctypes.c_int32),
-        ("C", ctypes.c_int32), ("pad0", ctypes.c_int32),
+        ("C", ctypes.c_int32), ("variant", ctypes.c_int32),
         ("off", _P), ("numel", _P),
         ("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
         ("eps", ctypes.c_float), ("wd", ctypes.c_float),
@@ -124,12 +124,14 @@ class Oracle:
     STATE_F32 = ("x", "m", "v", "v_fresh", "e_w", "e_s", "scale_w", "scale_s",
                  "c_bar", "r_prev", "c_cur", "R", "Sx", "Su")
 
-    def __init__(self, offsets, numels, W: int, chunk: int, hp: dict, x0: np.ndarray):
+    def __init__(self, offsets, numels, W: int, chunk: int, hp: dict, x0: np.ndarray,
+                 variant: int = 0):
         self.off = np.ascontiguousarray(offsets, dtype=np.int64)
         self.numel = np.ascontiguousarray(numels, dtype=np.int64)
         L = len(self.off)
         N = int(self.numel.sum())
         self.N, self.L, self.W, self.C = N, L, W, chunk
+        self.variant = int(variant)
         self.K = -(-N // chunk)
         self.NW = -(-N // 32)
         self.hp = dict(hp)
@@ -159,6 +161,7 @@ class Oracle:
         h = self.hp
         s = _OrcT()
         s.N, s.L, s.W, s.C = self.N, self.L, self.W, self.C
+        s.variant = self.variant
         s.off, s.numel = _p(self.off), _p(self.numel)
         s.lr, s.beta1, s.beta2 = h["lr"], h["beta1"], h["beta2"]
         s.eps, s.wd = h["eps"], h["weight_decay"]

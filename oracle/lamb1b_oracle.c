@@ -36,7 +36,10 @@
  *   tracked from g~; per tensor R = max (sqrt(v_frozen)+eps)/(sqrt(v_f)+eps);
  *   soft thresholds: r = clip(clip(R, fmin, fmax), (1-thr) r_prev,
  *   (1+thr) r_prev), c = c_bar * r with c_bar the exponential moving average of
- *   the warmup coefficients.  Parity with the published algorithm is unpinned
+ *   the warmup coefficients.  Variant 1 is 1-bit Adam (the 1-bit Adam page and
+ *   the 1-bit LAMB background on it): vanilla Adam in the warmup, the same
+ *   compressed momentum exchange in the compression stage, no layerwise
+ *   coefficient and no fresh variance.  Parity with the published algorithm is unpinned
  *   for those readings (bias correction, clip bounds, scale formula, c_bar,
  *   fresh variance, soft thresholds); the pins here are the stated invariants.
  *
@@ -54,7 +57,8 @@
 typedef struct {
     /* problem */
     int64_t N;
-    int32_t L, W, C, pad0;
+    int32_t L, W, C;
+    int32_t variant;        /* 0: 1-bit LAMB, 1: 1-bit Adam (no layerwise scaling) */
     const int64_t* off;     /* [L] first flat index of tensor l   */
     const int64_t* numel;   /* [L] element count of tensor l      */
     /* hyper-parameters */
@@ -206,6 +210,12 @@ int orc_warmup_step(orc_t* s, const float* g, int64_t ld)
     const float one_m_ema = fsub(1.0f, s->cema);
     for (int32_t l = 0; l < s->L; ++l) {
         int64_t lo = s->off[l], hi = lo + s->numel[l];
+        if (s->variant == 1) {
+            /* 1-bit Adam's warmup is vanilla Adam: no layerwise coefficient */
+            float gl = s->lr;
+            for (int64_t i = lo; i < hi; ++i) s->x[i] = fsub(s->x[i], fmul(gl, u[i]));
+            continue;
+        }
         float sx = orc_cpt_sumsq(s->x, 0, lo, hi);
         float su = orc_cpt_sumsq(u, 0, lo, hi);
         float ratio = (sx == 0.0f || su == 0.0f) ? 1.0f : fdiv(fsqrt(sx), fsqrt(su));
@@ -294,6 +304,11 @@ int orc_compress_chunk_step(orc_t* s, const float* g, int64_t ld, int64_t k, flo
         int64_t i = base + j;
         int pos = (words[j / 32] >> (j % 32)) & 1u;
         float m_new = pos ? ss : -ss;
+        if (s->variant == 1) {      /* 1-bit Adam: no fresh variance, no ratio */
+            s->m[i] = m_new;
+            if (rho) rho[j] = 1.0f;
+            continue;
+        }
         float gt = fdiv(fsub(m_new, fmul(s->beta1, s->m[i])), w1);
         s->v_fresh[i] = fadd(fmul(s->beta2, s->v_fresh[i]), fmul(w2, fmul(gt, gt)));
         float num = fadd(fsqrt(s->v[i]), s->eps);
@@ -337,6 +352,10 @@ int orc_compress_step(orc_t* s, const float* g, int64_t ld)
         orc_compress_chunk_step(s, g, ld, k, rho + k * C);
     for (int32_t l = 0; l < s->L; ++l) {
         int64_t lo = s->off[l], hi = lo + s->numel[l];
+        if (s->variant == 1) {      /* 1-bit Adam: coefficient 1, frozen-variance update */
+            update_tensor(s, l, 1.0f);
+            continue;
+        }
         float R = 0.0f;
         for (int64_t i = lo; i < hi; ++i) R = (rho[i] > R) ? rho[i] : R;
         float r = orc_layer_factor(R, s->r_prev[l], s->fmin, s->fmax, s->fthr);

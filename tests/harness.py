@@ -71,13 +71,14 @@ def close_vec_per_tensor(a, b, offsets, numels, tol):
 class Pair:
     """GPU optimizer and CPU oracle over the same workload."""
 
-    def __init__(self, wl, check_finite=0):
+    def __init__(self, wl, check_finite=0, variant=0):
         self.wl = wl
         self.x0 = workload.gen_params(wl)
         self.x = torch.from_numpy(self.x0.copy()).cuda()
-        hp = dict(wl.hp, check_finite=check_finite)
+        hp = dict(wl.hp, check_finite=check_finite, variant=variant)
         self.gpu = pkg.OneBitLamb(self.x, layers_of(wl), wl.W, wl.chunk, **hp)
-        self.orc = oracle.Oracle(wl.offsets, wl.numels, wl.W, wl.chunk, wl.hp, self.x0)
+        self.orc = oracle.Oracle(wl.offsets, wl.numels, wl.W, wl.chunk, wl.hp, self.x0,
+                                 variant=variant)
         self.ld = grad_ld(wl)
         self.t = 0
 

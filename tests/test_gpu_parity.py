@@ -17,8 +17,8 @@ def bert_mini(W=8, chunk=2048, grad="f32", **kw):
     return workload.custom("bert_mini", t, W=W, chunk=chunk, grad=grad, grad_std=1e-3, **kw)
 
 
-def run(wl, n_warm, n_comp, expect_bitwise=True):
-    p = Pair(wl)
+def run(wl, n_warm, n_comp, expect_bitwise=True, variant=0):
+    p = Pair(wl, variant=variant)
     diffs = 0
     for i in range(n_warm):
         p.warmup()
@@ -91,3 +91,18 @@ def test_many_tensors_in_one_chunk():
 
 def test_odd_worker_count_and_large_w():
     run(bert_mini(W=37, chunk=512), 1, 2)
+
+
+# ---- 1-bit Adam variant ------------------------------------------------------
+
+def test_adam_variant_tiny_and_bert_mini():
+    wl = workload.workloads()["tiny"]
+    run(wl, wl.warmup_steps, wl.compress_steps, variant=1)
+    run(bert_mini(W=8, chunk=2048), 4, 6, variant=1)
+
+
+def test_adam_variant_in_kernel_gradients():
+    t = workload.bert_tensors(1, 128, 512, 800)
+    wl = workload.custom("adam_w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
+                         fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
+    run(wl, 2, 2, variant=1)

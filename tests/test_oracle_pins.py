@@ -385,3 +385,64 @@ def test_workload_tables():
         assert off[0] == 0 and np.all(off[1:] == off[:-1] + num[:-1])
     large = workload.workloads()["large_w32"]
     assert int(large.layer_heavy.sum()) == 79
+
+
+# ---------------------------------------------------------------------------
+# 1-bit Adam variant (the predecessor method: Adam warmup, frozen-variance
+# compressed momentum, no layerwise coefficient)
+# ---------------------------------------------------------------------------
+
+def adam_bruteforce(x, grads, hp):
+    """Textbook Adam in float64 without bias correction, decoupled weight
+    decay inside the update, at the binary32 settings."""
+    hp = {k: float(np.float32(v)) for k, v in hp.items()}
+    x = x.astype(np.float64).copy()
+    m = np.zeros_like(x)
+    v = np.zeros_like(x)
+    for g in grads:
+        gb = g.astype(np.float64).mean(axis=0)
+        m = hp["beta1"] * m + (1 - hp["beta1"]) * gb
+        v = hp["beta2"] * v + (1 - hp["beta2"]) * gb * gb
+        x -= hp["lr"] * (m / (np.sqrt(v) + hp["eps"]) + hp["weight_decay"] * x)
+    return x, m, v
+
+
+@pytest.mark.parametrize("W", [1, 4])
+def test_adam_variant_warmup_equals_bruteforce_adam(W):
+    wl = workload.custom("bf", [("a", (40, 30)), ("b", (30,)), ("c", (700,))],
+                         W=W, chunk=256, grad_std=1e-2)
+    x0 = workload.gen_params(wl)
+    o = oracle.Oracle(wl.offsets, wl.numels, W, wl.chunk, HP, x0, variant=1)
+    grads = []
+    for t in range(6):
+        g = workload.grads_for_step(wl, t)
+        grads.append(g)
+        o.warmup_step(g)
+    xb, mb, vb = adam_bruteforce(x0, grads, HP)
+    for got, want in ((o.x, xb), (o.m, mb), (o.v, vb)):
+        assert np.max(np.abs(got - want)) <= 1e-5 * np.max(np.abs(want))
+    assert np.all(o.c_cur == 1.0) and np.all(o.c_bar == 1.0)
+
+
+def test_adam_variant_lossless_compression_is_frozen_variance_momentum_sgd():
+    """With exact 1-bit compression (constant-magnitude momentum chunks) a
+    1-bit Adam compression step is momentum SGD preconditioned by the frozen
+    variance, coefficient 1 (the 1-bit Adam page: variance frozen after the
+    warmup, momentum communicated with error-compensated compression)."""
+    rng = np.random.default_rng(12)
+    numel = [1024, 2048]
+    o = _fresh(numel, 2, 256, HP, x0=rng.standard_normal(3072).astype(np.float32))
+    o.variant = 1
+    o.v[:] = rng.uniform(1e-6, 1e-4, o.N).astype(np.float32)
+    o.freeze()
+    vf0 = o.v_fresh.copy()
+    x0 = o.x.astype(np.float64).copy()
+    a = np.float32(3e-3)
+    sg = np.where(rng.random(o.N) < 0.5, -1, 1)
+    o.compress_step(np.stack([a * sg, a * sg]).astype(np.float32))
+    m_w = (1 - 0.9) * a * sg
+    assert np.allclose(o.m, m_w, rtol=1e-6)
+    np.testing.assert_array_equal(o.v_fresh, vf0)      # no fresh variance
+    assert np.all(o.c_cur == 1.0)
+    u = m_w / (np.sqrt(o.v.astype(np.float64)) + 1e-6) + 0.01 * x0
+    np.testing.assert_allclose(o.x, x0 - 1e-3 * u, rtol=1e-6, atol=1e-9)
