@@ -112,7 +112,7 @@ struct Ring {
 
 // Producer side: issue the bulk copies of stream item j (tile i = j / TPC of
 // this CTA, kind r = j % TPC) into stage j % STAGES; called by thread 0 only.
-template <int TILE, int SG, int STAGES>
+template <int TILE, int SG, int STAGES, bool ADAM>
 __device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P, const Dev& D,
                                            const Grads& G, unsigned char* ring, uint64_t* full)
 {
@@ -142,7 +142,7 @@ __device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P,
             tma::load(a, static_cast<const unsigned char*>(G.ptr) + ((int64_t)w * G.ld + base) * SG,
                       gbytes, bar);
     } else if (r == W + 1) {
-        if (P.adam) {   // 1-bit Adam needs no second moment here
+        if constexpr (ADAM) {   // 1-bit Adam needs no second moment here
             tma::arrive_expect_tx(bar, R::kSlot);
             tma::load(a, D.e_s + base, R::kSlot, bar);
         } else {
@@ -190,7 +190,7 @@ struct MinBlocks {
     static constexpr int value = (STAGES * 2 * (NT * 4 * SLOTS) * 4 <= 100 * 1024) ? 2 : 1;
 };
 
-template <int NT, int SLOTS, int GK, int STAGES, int C>
+template <int NT, int SLOTS, int GK, int STAGES, int C, bool ADAM>
 __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
     k_compress(const Problem P, const Dev D, const Grads G)
 {
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = P.W;
-    const int TPC = W + (P.adam ? 2 : 3);               // stream items per tile
+    const int TPC = W + (ADAM ? 2 : 3);                 // stream items per tile
     const int64_t ntiles = P.Np / TILE;
     const int64_t nloc = (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
     const int64_t total = nloc * TPC;
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
     int64_t issued = 0, released = 0;
     if (tid == 0)
         for (; issued < total && issued < STAGES; ++issued)
-            issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+            issue_item<TILE, SG, STAGES, ADAM>(issued, TPC, P, D, G, ring, full);
 
     bool bad = false;        // non-finite gradient seen
     bool lost = false;       // a stage wait gave up
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             released += (w == 0) ? 2 : 1;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+                    issue_item<TILE, SG, STAGES, ADAM>(issued, TPC, P, D, G, ring, full);
             const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
             const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
             uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
@@ -382,7 +382,8 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
             const int64_t jS = j0 + W + 1, jF = j0 + W + 2;
             const int sS = (int)(jS % STAGES), sF = (int)(jF % STAGES);
             if (!wait_stage(&full[sS], (uint32_t)((jS / STAGES) & 1))) lost = true;
-            if (!P.adam && !wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
+            if constexpr (!ADAM)
+                if (!wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
             const float* es_in = reinterpret_cast<const float*>(ring + sS * R::kStage);
             const float* v_in = es_in + TILE;
             const float* vf_in = reinterpret_cast<const float*>(ring + sF * R::kStage);
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                 const int off = s * NT * 4 + tid * 4;
                 const float4 e = *reinterpret_cast<const float4*>(es_in + off);
                 const float ee[4] = {e.x, e.y, e.z, e.w};
-                if (!P.adam) {
+                if constexpr (!ADAM) {
                     const float4 v = *reinterpret_cast<const float4*>(v_in + off);
                     const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
                     vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
@@ -409,10 +410,10 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                 if (lane == 0) red[W & 1][s * NWARP + warp] = t;
             }
             if (__syncthreads_or(lost)) goto abort;
-            released += P.adam ? 1 : 2;
+            released += ADAM ? 1 : 2;
             if (tid == 0)
                 for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_item<TILE, SG, STAGES>(issued, TPC, P, D, G, ring, full);
+                    issue_item<TILE, SG, STAGES, ADAM>(issued, TPC, P, D, G, ring, full);
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
             const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
 
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                     nib |= (valid && pos) ? (1u << c) : 0u;
                     es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
                     mn[c] = valid ? sgn : 0.0f;
-                    if (P.adam) continue;
+                    if constexpr (ADAM) continue;
                     // reconstructed gradient and fresh second moment
                     const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
                     vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
@@ -459,7 +460,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                     D.signs_s[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
                 *reinterpret_cast<float4*>(D.e_s + base + off) = make_float4(es[0], es[1], es[2], es[3]);
                 *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-                if (!P.adam)
+                if constexpr (!ADAM)
                     *reinterpret_cast<float4*>(D.v_fresh + base + off) =
                         make_float4(vf[0], vf[1], vf[2], vf[3]);
             }
@@ -513,12 +514,12 @@ __global__ void k_factor(const Problem P, const Dev D)
 
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st);
 
-template <int NT, int SLOTS, int GK, int STAGES, int C>
+template <int NT, int SLOTS, int GK, int STAGES, int C, bool ADAM>
 static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     constexpr int TILE = NT * 4 * SLOTS;
     constexpr size_t smem = (size_t)STAGES * Ring<TILE>::kStage;
-    auto kern = k_compress<NT, SLOTS, GK, STAGES, C>;
+    auto kern = k_compress<NT, SLOTS, GK, STAGES, C, ADAM>;
     // per-device launch shape, computed once per instantiation
     static int cached_device = -1;
     static int grid_cap = 0;
@@ -540,14 +541,21 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
     return cudaGetLastError();
 }
 
+template <int NT, int SLOTS, int STAGES, int C, bool ADAM>
+static cudaError_t launch_grad(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
+{
+    switch (G.kind) {
+    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES, C, ADAM>(P, D, G, st);
+    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES, C, ADAM>(P, D, G, st);
+    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES, C, ADAM>(P, D, G, st);
+    }
+}
+
 template <int NT, int SLOTS, int STAGES, int C>
 static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
-    switch (G.kind) {
-    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES, C>(P, D, G, st);
-    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES, C>(P, D, G, st);
-    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES, C>(P, D, G, st);
-    }
+    return P.adam ? launch_grad<NT, SLOTS, STAGES, C, true>(P, D, G, st)
+                  : launch_grad<NT, SLOTS, STAGES, C, false>(P, D, G, st);
 }
 
 int64_t padded_length(int64_t N, int C)
