@@ -106,3 +106,43 @@ def test_adam_variant_in_kernel_gradients():
     wl = workload.custom("adam_w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
                          fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
     run(wl, 2, 2, variant=1)
+
+
+# ---- non-finite inputs ---------------------------------------------------------
+
+def test_nonfinite_gradients_propagate_like_the_oracle():
+    """A NaN and an Inf gradient in one worker's chunk: NaN sends +1 (sign
+    bit rule), the chunk's scale and errors become NaN, the server chunk
+    follows, the tensor's ratio max counts NaN as +Inf; every word and every
+    NaN position agrees with the oracle."""
+    import numpy as np
+    import torch
+    wl = bert_mini(W=4, chunk=1024)
+    p = Pair(wl)
+    for _ in range(2):
+        p.warmup()
+    p.freeze()
+    g_host = workload.grads_for_step(wl, p.t)
+    g_host[1, 5000] = np.nan
+    g_host[2, 70000] = np.inf
+    g_dev = torch.zeros((wl.W, p.ld), device="cuda")
+    g_dev[:, :wl.N] = torch.from_numpy(g_host).cuda()
+    p.gpu.compress_step(g_dev)
+    p.orc.compress_step(g_host)
+    p.t += 1
+    st = p.gpu_state()
+    o = p.orc
+    nw = st["nw"]
+    np.testing.assert_array_equal(st["signs_w"][:, :nw], o.signs_w)
+    np.testing.assert_array_equal(st["signs_s"][:nw], o.signs_s)
+    for k in ("m", "e_s", "v_fresh"):
+        np.testing.assert_array_equal(np.isnan(st[k][:wl.N]), np.isnan(getattr(o, k)), err_msg=k)
+        fin = ~np.isnan(getattr(o, k))
+        np.testing.assert_array_equal(st[k][:wl.N][fin], getattr(o, k)[fin], err_msg=k)
+    np.testing.assert_array_equal(np.isnan(st["e_w"][:, :wl.N]), np.isnan(o.e_w))
+    np.testing.assert_array_equal(np.isnan(st["scale_w"]), np.isnan(o.scale_w))
+    np.testing.assert_array_equal(np.isnan(st["x"]), np.isnan(o.x))
+    fin = ~np.isnan(o.x)
+    np.testing.assert_array_equal(st["x"][fin], o.x[fin])
+    assert np.isinf(o.R).any()
+    np.testing.assert_array_equal(st["R_last"], o.R)
