@@ -12,10 +12,11 @@
 // tile is 4096 elements = 4096/C chunks, or one 8192-element chunk).
 // Every input of a tile -- the old momentum, each worker's gradient and
 // error, then the server error, frozen and fresh second moments -- is copied
-// into a STAGES-deep ring of shared-memory stages by TMA bulk copies
-// (cp.async.bulk, completion on an mbarrier), issued by thread 0 as soon as a
-// stage is released, so the next tiles stream in while the CTA reduces and
-// stores the current one.  Outputs are written with coalesced 16-byte stores.
+// into a 7-slot ring of shared-memory slots by TMA bulk copies
+// (cp.async.bulk, completion on one mbarrier per slot), issued by thread 0 as
+// soon as enough slots are released, so the next arrays stream in while the
+// CTA reduces and stores the current one; while the server phase holds its
+// three arrays the next tile's momentum and first worker are already loading.  Outputs are written with coalesced 16-byte stores.
 //
 // Thread map: thread `tid` of an NT-thread CTA holds SLOTS aligned float4
 // groups, group s at chunk offset s*NT*4 + tid*4.  Warp w's lanes therefore
@@ -100,60 +101,84 @@ __device__ __forceinline__ uint32_t pack_nibbles(uint32_t nib, int lane)
 template <int GK>
 struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGradBF16 ? 2 : 0); };
 
-// Per-stage layout: slot A (TILE floats) then slot B (TILE floats).  Per tile
-// (TILE consecutive elements = TILE/C whole chunks, or exactly one chunk when
-// C == TILE), the tiles streamed in order are: M (m_old -> A), W worker tiles
-// (g_w -> A, e_w -> B), S (e_s -> A, v -> B), F (v_fresh -> A).
+// Ring of NSLOT shared-memory slots of TILE floats, one mbarrier per slot.
+// Every tile streams, in slot positions: M (m_old), then per worker W_w its
+// gradients (when stored) and its error, then S (e_s, and v for 1-bit LAMB),
+// then F (v_fresh, 1-bit LAMB only).  Slot position p lives in slot p % NSLOT
+// and completes phase (p / NSLOT) of that slot's barrier.
 template <int TILE>
 struct Ring {
     static constexpr uint32_t kSlot = TILE * 4;
-    static constexpr uint32_t kStage = 2 * kSlot;
 };
 
-// Producer side: issue the bulk copies of stream item j (tile i = j / TPC of
-// this CTA, kind r = j % TPC) into stage j % STAGES; called by thread 0 only.
-template <int TILE, int SG, int STAGES, bool ADAM>
-__device__ __forceinline__ void issue_item(int64_t j, int TPC, const Problem& P, const Dev& D,
-                                           const Grads& G, unsigned char* ring, uint64_t* full)
+template <int SG, bool ADAM>
+struct Stream {
+    static constexpr int kPerWorker = SG > 0 ? 2 : 1;
+    static constexpr int kServer = ADAM ? 1 : 2;         // slots of item S
+    __device__ static int items(int W) { return W + (ADAM ? 2 : 3); }
+    // slots of item r
+    __device__ static int slots(int r, int W) { return r == 0 ? 1 : (r <= W ? kPerWorker : (r == W + 1 ? kServer : 1)); }
+};
+
+// A slot position kept as (slot, barrier phase), advanced without division.
+template <int NSLOT>
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ RingPos plus(int n) const
+    {
+        RingPos q = *this;
+        q.slot += n;
+        if (q.slot >= NSLOT) { q.slot -= NSLOT; q.phase ^= 1u; }
+        return q;
+    }
+};
+
+// Producer side: issue the bulk copies of item r of tile t whose first slot
+// position is p; called by thread 0 only.
+template <int TILE, int SG, int NSLOT, bool ADAM>
+__device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, const Problem& P,
+                                           const Dev& D, const Grads& G, unsigned char* ring,
+                                           uint64_t* full)
 {
     using R = Ring<TILE>;
     const int W = P.W;
-    const int64_t i = j / TPC;
-    const int r = (int)(j - i * TPC);
-    const int64_t t = blockIdx.x + i * gridDim.x;
     const int64_t base = t * TILE;
-    const int st = (int)(j % STAGES);
-    unsigned char* a = ring + st * R::kStage;
-    unsigned char* b = a + R::kSlot;
-    uint64_t* bar = &full[st];
+    auto copy = [&](int k, const void* src, uint32_t bytes) {
+        const int sl = p.plus(k).slot;
+        tma::arrive_expect_tx(&full[sl], bytes);
+        tma::load(ring + (uint32_t)sl * R::kSlot, src, bytes, &full[sl]);
+    };
     if (r == 0) {
-        tma::arrive_expect_tx(bar, R::kSlot);
-        tma::load(a, D.m + base, R::kSlot, bar);
+        copy(0, D.m + base, R::kSlot);
     } else if (r <= W) {
         const int w = r - 1;
-        uint32_t gbytes = 0;
         if constexpr (SG > 0) {
             const int64_t n_t = (base + TILE <= P.N) ? (int64_t)TILE : P.N - base;
-            gbytes = (uint32_t)(((n_t * SG) + 15) / 16 * 16);
-        }
-        tma::arrive_expect_tx(bar, R::kSlot + gbytes);
-        tma::load(b, D.e_w + (int64_t)w * P.Np + base, R::kSlot, bar);
-        if constexpr (SG > 0)
-            tma::load(a, static_cast<const unsigned char*>(G.ptr) + ((int64_t)w * G.ld + base) * SG,
-                      gbytes, bar);
-    } else if (r == W + 1) {
-        if constexpr (ADAM) {   // 1-bit Adam needs no second moment here
-            tma::arrive_expect_tx(bar, R::kSlot);
-            tma::load(a, D.e_s + base, R::kSlot, bar);
+            const uint32_t gbytes = (uint32_t)(((n_t * SG) + 15) / 16 * 16);
+            copy(0, static_cast<const unsigned char*>(G.ptr) + ((int64_t)w * G.ld + base) * SG, gbytes);
+            copy(1, D.e_w + (int64_t)w * P.Np + base, R::kSlot);
         } else {
-            tma::arrive_expect_tx(bar, 2 * R::kSlot);
-            tma::load(a, D.e_s + base, R::kSlot, bar);
-            tma::load(b, D.v + base, R::kSlot, bar);
+            copy(0, D.e_w + (int64_t)w * P.Np + base, R::kSlot);
         }
+    } else if (r == W + 1) {
+        copy(0, D.e_s + base, R::kSlot);
+        if constexpr (!ADAM) copy(1, D.v + base, R::kSlot);
     } else {
-        tma::arrive_expect_tx(bar, R::kSlot);
-        tma::load(a, D.v_fresh + base, R::kSlot, bar);
+        copy(0, D.v_fresh + base, R::kSlot);
     }
+}
+
+// Consumer side: wait for n consecutive slots starting at p.
+template <int NSLOT>
+__device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int n)
+{
+    bool ok = true;
+    for (int k = 0; k < n; ++k) {
+        const RingPos<NSLOT> q = p.plus(k);
+        ok &= wait_stage(&full[q.slot], q.phase);
+    }
+    return ok;
 }
 
 // Chunk totals from the tile's 128-leaf partials red[0 .. NPART) (element
@@ -185,13 +210,13 @@ __device__ __forceinline__ float chunk_totals(const float* red, int lane)
 }
 
 // Two CTAs per SM when two rings fit in shared memory, else one.
-template <int NT, int SLOTS, int STAGES>
+template <int NT, int SLOTS, int NSLOT>
 struct MinBlocks {
-    static constexpr int value = (STAGES * 2 * (NT * 4 * SLOTS) * 4 <= 100 * 1024) ? 2 : 1;
+    static constexpr int value = (NSLOT * (NT * 4 * SLOTS) * 4 <= 112 * 1024) ? 2 : 1;
 };
 
-template <int NT, int SLOTS, int GK, int STAGES, int C, bool ADAM>
-__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
+template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM>
+__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
     k_compress(const Problem P, const Dev D, const Grads G)
 {
     constexpr int NWARP = NT / 32;
@@ -204,30 +229,44 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
     constexpr int SG = GradBytes<GK>::value;
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;
+    using SL = Stream<SG, ADAM>;
     extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ uint64_t full[STAGES];
+    __shared__ uint64_t full[NSLOT];
     __shared__ float red[2][NPART];
     __shared__ uint32_t lmax[kMaxChunkLayers];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = P.W;
-    const int TPC = W + (ADAM ? 2 : 3);                 // stream items per tile
+    const int TPC = SL::items(W);                       // stream items per tile
     const int64_t ntiles = P.Np / TILE;
     const int64_t nloc = (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
-    const int64_t total = nloc * TPC;
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) tma::bar_init(&full[s], 1);
+        for (int s = 0; s < NSLOT; ++s) tma::bar_init(&full[s], 1);
         tma::fence_init();
     }
     for (int i = tid; i < kMaxChunkLayers; i += NT) lmax[i] = 0u;
     __syncthreads();
 
-    // ---- producer (thread 0): item j goes to stage j % STAGES --------------
-    int64_t issued = 0, released = 0;
-    if (tid == 0)
-        for (; issued < total && issued < STAGES; ++issued)
-            issue_item<TILE, SG, STAGES, ADAM>(issued, TPC, P, D, G, ring, full);
+    // ---- producer (thread 0): items in order, as long as all their slots
+    // fit in the ring ahead of the released slot positions ------------------
+    int issue_pos = 0, released = 0;          // slot positions (per CTA)
+    int64_t issue_tile = 0;                   // local tile index of the next item
+    int issue_r = 0;                          // its kind
+    RingPos<NSLOT> ip;                        // its first slot
+    auto issue_ready = [&]() {
+        while (issue_tile < nloc) {
+            const int n = SL::slots(issue_r, W);
+            if (issue_pos + n > released + NSLOT) break;
+            issue_item<TILE, SG, NSLOT, ADAM>(blockIdx.x + issue_tile * gridDim.x, issue_r, ip,
+                                              P, D, G, ring, full);
+            issue_pos += n;
+            ip = ip.plus(n);
+            if (++issue_r == TPC) { issue_r = 0; ++issue_tile; }
+        }
+    };
+    if (tid == 0) issue_ready();
+    RingPos<NSLOT> cp;                        // consumer: next slot to read
 
     bool bad = false;        // non-finite gradient seen
     bool lost = false;       // a stage wait gave up
@@ -236,7 +275,6 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
         const int64_t tile = blockIdx.x + ti * gridDim.x;
         const int64_t base = tile * TILE;
         const bool full_tile = base + TILE <= P.N;
-        const int64_t j0 = ti * TPC;
         const int64_t k0 = base / C;                     // first chunk of the tile
         const int64_t klast = (k0 + CPT - 1 < P.K - 1) ? k0 + CPT - 1 : P.K - 1;
         const int l0 = D.chunk_l0[k0];
@@ -280,9 +318,9 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
         // ---- item M: beta1 * m_old, kept for the whole tile ------------------
         float bm[SLOTS][4], acc[SLOTS][4];
         {
-            const int st = (int)(j0 % STAGES);
-            if (!wait_stage(&full[st], (uint32_t)((j0 / STAGES) & 1))) lost = true;
-            const float* a = reinterpret_cast<const float*>(ring + st * R::kStage);
+            if (!wait_slots<NSLOT>(full, cp, 1)) lost = true;
+            const float* a = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
+            cp = cp.plus(1);
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
                 const float4 mo = *reinterpret_cast<const float4*>(a + s * NT * 4 + tid * 4);
@@ -295,11 +333,11 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
 
         // ---- phase 1: every worker compresses its chunks ----------------------
         for (int w = 0; w < W; ++w) {
-            const int64_t j = j0 + 1 + w;
-            const int st = (int)(j % STAGES);
-            if (!wait_stage(&full[st], (uint32_t)((j / STAGES) & 1))) lost = true;
-            const unsigned char* a = ring + st * R::kStage;
-            const float* eb = reinterpret_cast<const float*>(a + R::kSlot);
+            if (!wait_slots<NSLOT>(full, cp, SL::kPerWorker)) lost = true;
+            const unsigned char* a = ring + (uint32_t)cp.slot * R::kSlot;
+            const float* eb = reinterpret_cast<const float*>(
+                ring + (uint32_t)cp.plus(SL::kPerWorker - 1).slot * R::kSlot);
+            cp = cp.plus(SL::kPerWorker);
             float z[SLOTS][4];
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
@@ -346,10 +384,8 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                 if (lane == 0) red[w & 1][s * NWARP + warp] = t;
             }
             if (__syncthreads_or(lost)) goto abort;
-            released += (w == 0) ? 2 : 1;
-            if (tid == 0)
-                for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_item<TILE, SG, STAGES, ADAM>(issued, TPC, P, D, G, ring, full);
+            released += (w == 0) ? 1 + SL::kPerWorker : SL::kPerWorker;
+            if (tid == 0) issue_ready();
             const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
             const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
             uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
@@ -379,14 +415,12 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
 
         // ---- phases 2 and 3: server average, recompression, scatter ----------
         {
-            const int64_t jS = j0 + W + 1, jF = j0 + W + 2;
-            const int sS = (int)(jS % STAGES), sF = (int)(jF % STAGES);
-            if (!wait_stage(&full[sS], (uint32_t)((jS / STAGES) & 1))) lost = true;
-            if constexpr (!ADAM)
-                if (!wait_stage(&full[sF], (uint32_t)((jF / STAGES) & 1))) lost = true;
-            const float* es_in = reinterpret_cast<const float*>(ring + sS * R::kStage);
-            const float* v_in = es_in + TILE;
-            const float* vf_in = reinterpret_cast<const float*>(ring + sF * R::kStage);
+            const int nsrv = SL::kServer + (ADAM ? 0 : 1);      // S (and F) slots
+            if (!wait_slots<NSLOT>(full, cp, nsrv)) lost = true;
+            const float* es_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
+            const float* v_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(1).slot * R::kSlot);
+            const float* vf_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(2).slot * R::kSlot);
+            cp = cp.plus(nsrv);
             float y[SLOTS][4], vz[SLOTS][4], vfo[SLOTS][4];
             const float Wf = (float)W;
 #pragma unroll
@@ -410,10 +444,8 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, STAGES>::value))
                 if (lane == 0) red[W & 1][s * NWARP + warp] = t;
             }
             if (__syncthreads_or(lost)) goto abort;
-            released += ADAM ? 1 : 2;
-            if (tid == 0)
-                for (; issued < total && issued < released + STAGES; ++issued)
-                    issue_item<TILE, SG, STAGES, ADAM>(issued, TPC, P, D, G, ring, full);
+            released += nsrv;
+            if (tid == 0) issue_ready();
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
             const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
 
@@ -488,9 +520,14 @@ abort:
     // CTA still has in flight land (bounded), then leave.
     if (tid == 0) {
         atomicOr(D.flags, 2u);
-        const int64_t first = issued > STAGES ? issued - STAGES : 0;
-        for (int64_t j = first; j < issued; ++j)
-            wait_stage(&full[j % STAGES], (uint32_t)((j / STAGES) & 1));
+        // every slot position issued but not yet released (at most NSLOT):
+        // they end at the producer's position ip
+        RingPos<NSLOT> q = ip;
+        for (int k = issue_pos - released; k > 0; --k) {
+            q.slot -= 1;
+            if (q.slot < 0) { q.slot += NSLOT; q.phase ^= 1u; }
+            wait_stage(&full[q.slot], q.phase);
+        }
     }
     __syncthreads();
 }
@@ -514,12 +551,12 @@ __global__ void k_factor(const Problem P, const Dev D)
 
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st);
 
-template <int NT, int SLOTS, int GK, int STAGES, int C, bool ADAM>
+template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM>
 static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     constexpr int TILE = NT * 4 * SLOTS;
-    constexpr size_t smem = (size_t)STAGES * Ring<TILE>::kStage;
-    auto kern = k_compress<NT, SLOTS, GK, STAGES, C, ADAM>;
+    constexpr size_t smem = (size_t)NSLOT * Ring<TILE>::kSlot;
+    auto kern = k_compress<NT, SLOTS, GK, NSLOT, C, ADAM>;
     // per-device launch shape, computed once per instantiation
     static int cached_device = -1;
     static int grid_cap = 0;
@@ -528,6 +565,9 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
     if (e != cudaSuccess) return e;
     if (cached_device != dev) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return e;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      cudaSharedmemCarveoutMaxShared)))
             return e;
         int per_sm = 0, sms = 0;
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem))) return e;
@@ -541,21 +581,21 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
     return cudaGetLastError();
 }
 
-template <int NT, int SLOTS, int STAGES, int C, bool ADAM>
+template <int NT, int SLOTS, int NSLOT, int C, bool ADAM>
 static cudaError_t launch_grad(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     switch (G.kind) {
-    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, STAGES, C, ADAM>(P, D, G, st);
-    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, STAGES, C, ADAM>(P, D, G, st);
-    default:        return launch_one<NT, SLOTS, kGradPhilox, STAGES, C, ADAM>(P, D, G, st);
+    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, NSLOT, C, ADAM>(P, D, G, st);
+    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, NSLOT, C, ADAM>(P, D, G, st);
+    default:        return launch_one<NT, SLOTS, kGradPhilox, NSLOT, C, ADAM>(P, D, G, st);
     }
 }
 
-template <int NT, int SLOTS, int STAGES, int C>
+template <int NT, int SLOTS, int NSLOT, int C>
 static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
-    return P.adam ? launch_grad<NT, SLOTS, STAGES, C, true>(P, D, G, st)
-                  : launch_grad<NT, SLOTS, STAGES, C, false>(P, D, G, st);
+    return P.adam ? launch_grad<NT, SLOTS, NSLOT, C, true>(P, D, G, st)
+                  : launch_grad<NT, SLOTS, NSLOT, C, false>(P, D, G, st);
 }
 
 int64_t padded_length(int64_t N, int C)
@@ -572,12 +612,12 @@ cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, floa
     // 4096-element tiles (256 threads x 4 float4 groups) holding 4096/C chunks;
     // 8192-element chunks use 512-thread tiles of one chunk.
     switch (P.C) {
-    case 256:  e = launch_kind<256, 4, 3, 256>(P, D, G, st); break;
-    case 512:  e = launch_kind<256, 4, 3, 512>(P, D, G, st); break;
-    case 1024: e = launch_kind<256, 4, 3, 1024>(P, D, G, st); break;
-    case 2048: e = launch_kind<256, 4, 3, 2048>(P, D, G, st); break;
-    case 4096: e = launch_kind<256, 4, 3, 4096>(P, D, G, st); break;
-    case 8192: e = launch_kind<512, 4, 3, 8192>(P, D, G, st); break;
+    case 256:  e = launch_kind<256, 4, 7, 256>(P, D, G, st); break;
+    case 512:  e = launch_kind<256, 4, 7, 512>(P, D, G, st); break;
+    case 1024: e = launch_kind<256, 4, 7, 1024>(P, D, G, st); break;
+    case 2048: e = launch_kind<256, 4, 7, 2048>(P, D, G, st); break;
+    case 4096: e = launch_kind<256, 4, 7, 4096>(P, D, G, st); break;
+    case 8192: e = launch_kind<512, 4, 7, 8192>(P, D, G, st); break;
     default:   return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
