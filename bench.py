@@ -392,6 +392,22 @@ def run_ours(args, world, rank, local):
     achieved = kb / (k_avg / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
 
+    # per-tensor coefficients after the timed steps: where the soft thresholds
+    # and clip bounds are active
+    sv = opt.state()
+    r_now = sv["r_prev"].cpu().numpy()
+    c_now = sv["c_cur"].cpu().numpy()
+    cbar_now = sv["c_bar"].cpu().numpy()
+    hp = wl.hp
+    layer_stats = {
+        "r_at_factor_max": int(np.sum(r_now >= np.float32(hp["factor_max"]))),
+        "r_at_factor_min": int(np.sum(r_now <= np.float32(hp["factor_min"]))),
+        "r_min": float(r_now.min()), "r_max": float(r_now.max()),
+        "c_min": float(c_now.min()), "c_max": float(c_now.max()),
+        "c_bar_at_clip": int(np.sum((cbar_now <= np.float32(hp["coeff_min"]))
+                                    | (cbar_now >= np.float32(hp["coeff_max"])))),
+        "tensors": int(len(r_now))}
+
     # ---- end to end through the public API with host buffers ----------------
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -426,7 +442,8 @@ def run_ours(args, world, rank, local):
                           "moments_kernel_ms": statistics.mean(warm_kernel_ms[1:] or warm_kernel_ms),
                           "params_per_s": N / (statistics.mean(warm_ms[1:] or warm_ms) / 1e3),
                           "steps": len(warm_ms)} if warm_ms else None),
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 if args.variant == "adam" else 3) * args.steps,
+        "layer_stats": layer_stats,
         "clocks": clocks,
         "e2e": e2e,
     }

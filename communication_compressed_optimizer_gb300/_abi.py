@@ -13,8 +13,8 @@ from . import build as _build
 _P = ctypes.c_void_p
 
 LAMB1B_OK = 0
-ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_STATE, ERR_CUDA, ERR_NONFINITE, ERR_DEVICE = \
-    -1, -2, -3, -4, -5, -6, -7
+ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_STATE, ERR_CUDA, ERR_NONFINITE, ERR_DEVICE, ERR_TIMEOUT = \
+    -1, -2, -3, -4, -5, -6, -7, -8
 GRAD_F32, GRAD_BF16, GRAD_PHILOX = 0, 1, 2
 
 EXPORTED = ("lamb1b_workspace_bytes", "lamb1b_init", "lamb1b_warmup_step",

@@ -7,6 +7,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "lamb1b.h"
 #include "lamb1b_internal.cuh"
@@ -102,6 +103,13 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
 }
 
 int grads_check(const lamb1b_ctx* ctx, const lamb1b_grads* g);
+
+// NVTX range around the host side of one stage (enqueue only), so profiler
+// timelines show which library call launched which kernels.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 }  // namespace
 
@@ -304,6 +312,7 @@ extern "C" int lamb1b_warmup_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, vo
     if (rc) return rc;
     if ((rc = grads_check(ctx, grads))) return rc;
     const Grads G = to_grads(ctx, grads);
+    NvtxRange range("lamb1b warmup step");
     if (lamb1b::launch_warmup(ctx->P, ctx->D, G, ctx->x, static_cast<cudaStream_t>(stream),
                               ctx->n_warm == 0, ctx->tracing ? ctx->ev : nullptr) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
@@ -318,6 +327,7 @@ extern "C" int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream)
     if (ctx->stage != 0) return LAMB1B_ERR_STATE;
     int rc = device_check(ctx);
     if (rc) return rc;
+    NvtxRange range("lamb1b freeze variance");
     if (lamb1b::launch_freeze(ctx->P, ctx->D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
     ctx->stage = 1;
@@ -332,6 +342,7 @@ extern "C" int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, 
     if (rc) return rc;
     if ((rc = grads_check(ctx, grads))) return rc;
     const Grads G = to_grads(ctx, grads);
+    NvtxRange range("lamb1b compression step");
     if (lamb1b::launch_compress(ctx->P, ctx->D, G, ctx->x, static_cast<cudaStream_t>(stream),
                                 ctx->tracing ? ctx->ev : nullptr) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
@@ -376,11 +387,11 @@ extern "C" int lamb1b_check_status(lamb1b_ctx* ctx, void* stream)
     if (cudaMemcpyAsync(&flags, ctx->D.flags, sizeof(flags), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
-    if (flags & 1u) {
+    if (flags & 3u) {
         if (cudaMemsetAsync(ctx->D.flags, 0, sizeof(uint32_t), st) != cudaSuccess ||
             cudaStreamSynchronize(st) != cudaSuccess)
             return LAMB1B_ERR_CUDA;
-        return LAMB1B_ERR_NONFINITE;
+        return (flags & 2u) ? LAMB1B_ERR_TIMEOUT : LAMB1B_ERR_NONFINITE;
     }
     return LAMB1B_OK;
 }
@@ -418,6 +429,7 @@ extern "C" const char* lamb1b_error_string(int code)
     case LAMB1B_ERR_CUDA: return "CUDA runtime error";
     case LAMB1B_ERR_NONFINITE: return "non-finite gradient seen";
     case LAMB1B_ERR_DEVICE: return "current device is not the context's device";
+    case LAMB1B_ERR_TIMEOUT: return "a kernel gave up waiting for its bulk copies";
     default: return "unknown error";
     }
 }

@@ -54,7 +54,10 @@ enum {
     LAMB1B_ERR_STATE = -4,      /* call out of order: init, warmup*, freeze, compress* */
     LAMB1B_ERR_CUDA = -5,       /* a CUDA runtime call or launch failed         */
     LAMB1B_ERR_NONFINITE = -6,  /* check_finite saw a NaN/Inf gradient          */
-    LAMB1B_ERR_DEVICE = -7      /* current device differs from the context's    */
+    LAMB1B_ERR_DEVICE = -7,     /* current device differs from the context's    */
+    LAMB1B_ERR_TIMEOUT = -8     /* a kernel gave up waiting for its own bulk copies
+                                   (bounded wait; never expected); the step's
+                                   results are not valid                        */
 };
 
 /* One tensor of the model ("each tensor has its own scaling coefficient",
@@ -207,9 +210,10 @@ int lamb1b_state_view(const lamb1b_ctx* ctx, lamb1b_state* out);
  * workspace through lamb1b_state_view (checkpoint resume).  stage 0 or 1. */
 int lamb1b_set_counters(lamb1b_ctx* ctx, int64_t t, int32_t n_warmup, int32_t stage);
 
-/* Synchronises `stream` and reports (then clears) the non-finite-gradient
- * flag raised by steps run with check_finite = 1: LAMB1B_ERR_NONFINITE if any
- * step since the last check saw a NaN or Inf gradient, else 0. */
+/* Synchronises `stream` and reports (then clears) the device status flags
+ * raised since the last check: LAMB1B_ERR_TIMEOUT if a compression kernel gave
+ * up waiting for its own shared-memory bulk copies, else LAMB1B_ERR_NONFINITE
+ * if a step run with check_finite = 1 saw a NaN or Inf gradient, else 0. */
 int lamb1b_check_status(lamb1b_ctx* ctx, void* stream);
 
 /* Tracing: with n == 4, every later warmup or compression step records

@@ -65,7 +65,7 @@ def test_workspace_bytes_and_validation():
     bad = [dict(W=0), dict(W=257), dict(chunk=100), dict(chunk=384), dict(chunk=16384),
            dict(beta1=1.0), dict(beta2=1.5), dict(eps=-1.0), dict(coeff_min=2.0, coeff_max=1.0),
            dict(factor_min=5.0), dict(factor_threshold=-0.1), dict(lr=float("nan")),
-           dict(check_finite=2)]
+           dict(check_finite=2), dict(variant=2)]
     for kw in bad:
         assert L.lamb1b_workspace_bytes(arr, 4, ctypes.byref(_hp(**kw))) == 0, kw
     # tables: gaps, overlaps, empty tensors, no tensors
@@ -108,7 +108,7 @@ def test_null_context_calls():
     assert L.lamb1b_set_counters(None, 0, 0, 0) == _abi.ERR_ARG
     assert L.lamb1b_check_status(None, None) == _abi.ERR_ARG
     assert L.lamb1b_destroy(None) == 0
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert L.lamb1b_error_string(code)
     assert L.lamb1b_gen_params(None, 0, 10, 1.0, 0, None) == _abi.ERR_ARG
 

@@ -181,3 +181,80 @@ def test_full_size_compression_step_sampled(name):
             assert R[l] >= o.R[j] * (1 - SCALAR_TOL), (l, R[l], o.R[j])
     assert n_whole >= 50
     opt.close()
+
+
+@pytest.mark.parametrize("name", ["base", "large", "large_w32", "gpt2xl"])
+def test_full_size_warmup_step_sampled(name):
+    """One LAMB warmup step at full size from a seeded synthetic state
+    (parameters, momentum, second moment): every sampled chunk's m and v, and
+    for whole small tensors the sums of squares, trust ratio, c_bar and the
+    updated parameters, against the oracle on the sampled chunks."""
+    wl = workload.workloads()[name]
+    N, W, C, L = wl.N, wl.W, wl.chunk, wl.L
+    free, _ = torch.cuda.mem_get_info()
+    gbytes = {"f32": 4, "bf16": 2, "philox": 0}[wl.grad]
+    need = pkg.workspace_bytes(layers_of(wl), W, C) + 4 * N + gbytes * W * (N + 8)
+    if need > 0.9 * free:
+        pytest.skip(f"needs {need / 1e9:.0f} GB of device memory")
+    x = torch.empty(N, device="cuda")
+    pkg.gen_params(x, 0, N, wl.param_std, wl.seed)
+    opt = pkg.OneBitLamb(x, layers_of(wl), W, C, **wl.hp)
+    st = opt.state()
+    pkg.gen_params(st["m"], 0, N, STDS["m"], SEEDS["m"])
+    pkg.gen_params(st["v"], 0, N, STDS["v"], SEEDS["v"])
+    st["v"][:N].mul_(st["v"][:N])
+    st["c_bar"].copy_(torch.from_numpy(c_bar_of(L)))
+    opt.set_counters(STEP, 3, 0)          # mid-warmup: c_bar follows its EMA
+    if wl.grad == "philox":
+        g = pkg.PhiloxGrads(wl.seed, wl.layer_std, wl.layer_heavy, wl.heavy_scale)
+    else:
+        q = 8 if wl.grad == "bf16" else 4
+        ld = -(-N // q) * q
+        g = torch.empty((W, ld), dtype=torch.int16 if wl.grad == "bf16" else torch.float32,
+                        device="cuda")
+        pkg.gen_grads(g, STEP, wl.seed, layers_of(wl), wl.layer_std, None, wl.heavy_scale)
+    opt.warmup_step(g)
+    torch.cuda.synchronize()
+    del g
+
+    ks = sample_chunks(wl, small=2 * C)
+    frags, NL = fragments(wl, ks)
+    idx = np.concatenate([np.arange(k * C, min((k + 1) * C, N)) for k in ks])
+    runs = [(k * C, min((k + 1) * C, N)) for k in ks]
+
+    def gather_host(fn):
+        return np.concatenate([fn(lo, hi) for lo, hi in runs])
+
+    x0 = gather_host(lambda lo, hi: host_normal(wl.seed, wl.param_std, lo, hi))
+    o = oracle.Oracle([f[1] for f in frags], [f[2] for f in frags], W, C, wl.hp, x0)
+    o.m[:] = gather_host(lambda lo, hi: host_normal(SEEDS["m"], STDS["m"], lo, hi))
+    v = gather_host(lambda lo, hi: host_normal(SEEDS["v"], STDS["v"], lo, hi))
+    o.v[:] = v * v
+    cb = c_bar_of(L)
+    o.c_bar[:] = [cb[f[0]] for f in frags]
+    o.t, o.n_warm = STEP, 3
+    gh = np.empty((W, NL), np.float32)
+    for w in range(W):
+        gw = gather_host(lambda lo, hi: workload.gen_grads_range(wl, STEP, w, lo, hi))
+        gh[w] = workload.bf16_round(gw) if wl.grad == "bf16" else gw
+    o.warmup_step(gh)
+
+    s = opt.state()
+    it = torch.from_numpy(idx).cuda()
+    for k in ("m", "v"):
+        np.testing.assert_array_equal(s[k][it].cpu().numpy().view(np.uint32),
+                                      getattr(o, k).view(np.uint32), err_msg=k)
+    Sx, Su = s["Sx"].cpu().numpy(), s["Su"].cpu().numpy()
+    c, cbar = s["c_cur"].cpu().numpy(), s["c_bar"].cpu().numpy()
+    xg = x[it].cpu().numpy()
+    n_whole = 0
+    for j, (l, lo, n, whole) in enumerate(frags):
+        if not whole:
+            continue
+        n_whole += 1
+        assert close_scalar(Sx[l], o.Sx[j]) and close_scalar(Su[l], o.Su[j]), l
+        assert close_scalar(c[l], o.c_cur[j]) and close_scalar(cbar[l], o.c_bar[j]), l
+        np.testing.assert_array_equal(xg[lo:lo + n].view(np.uint32),
+                                      o.x[lo:lo + n].view(np.uint32), err_msg=str(l))
+    assert n_whole >= 50
+    opt.close()

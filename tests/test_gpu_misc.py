@@ -40,8 +40,9 @@ def test_device_generator_matches_host_generator():
 
 
 def test_device_philox_stream_many_counters():
-    """2^22 consecutive counters of one stream, device vs host."""
-    wl = workload.custom("one", [("a", (1 << 22,))], W=1, chunk=256, grad_std=1.0)
+    """2^24 consecutive elements (2^22 Philox counters) of one stream, device
+    vs host, bit for bit."""
+    wl = workload.custom("one", [("a", (1 << 24,))], W=1, chunk=256, grad_std=1.0)
     out = torch.empty((1, wl.N), device="cuda")
     pkg.gen_grads(out, 3, 12345, layers_of(wl), wl.layer_std)
     wl.seed = 12345
