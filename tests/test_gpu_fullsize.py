@@ -12,6 +12,8 @@ tolerance, and for completely covered tensors the max ratio, factor,
 coefficient and updated parameters.  For the other tensors the GPU's max
 ratio must bound the sampled ratios from above.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -83,6 +85,8 @@ def fragments(wl, ks):
 def test_full_size_compression_step_sampled(name):
     wl = workload.workloads()[name]
     N, W, C, K, L = wl.N, wl.W, wl.chunk, wl.K, wl.L
+    gc.collect()
+    torch.cuda.empty_cache()              # earlier full-size tests' cached blocks
     free, _ = torch.cuda.mem_get_info()
     gbytes = {"f32": 4, "bf16": 2, "philox": 0}[wl.grad]
     need = pkg.workspace_bytes(layers_of(wl), W, C) + 4 * N + gbytes * W * (N + 8)
@@ -191,6 +195,8 @@ def test_full_size_warmup_step_sampled(name):
     updated parameters, against the oracle on the sampled chunks."""
     wl = workload.workloads()[name]
     N, W, C, L = wl.N, wl.W, wl.chunk, wl.L
+    gc.collect()
+    torch.cuda.empty_cache()              # earlier full-size tests' cached blocks
     free, _ = torch.cuda.mem_get_info()
     gbytes = {"f32": 4, "bf16": 2, "philox": 0}[wl.grad]
     need = pkg.workspace_bytes(layers_of(wl), W, C) + 4 * N + gbytes * W * (N + 8)
