@@ -339,6 +339,30 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                 ring + (uint32_t)cp.plus(SL::kPerWorker - 1).slot * R::kSlot);
             cp = cp.plus(SL::kPerWorker);
             float z[SLOTS][4];
+            // in-kernel gradients: the normal draws of all slots first, as
+            // independent Philox chains (instruction-level parallelism), then
+            // the Student-t draws of the heavy-tailed tensors' elements
+            float gin[SLOTS][4];
+            if constexpr (GK == kGradPhilox) {
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    gen::grads_normal4(G.seed, (uint64_t)(base + s * NT * 4 + tid * 4) >> 2, G.t,
+                                       (uint32_t)w, gin[s]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) gin[s][c] = fmul(stdv[s][c], gin[s][c]);
+                }
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    if (heavy[s]) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if ((heavy[s] >> c) & 1u)
+                                gin[s][c] = fmul(G.heavy_scale,
+                                                 gen::student_t3(G.seed, base + s * NT * 4 + tid * 4 + c,
+                                                                 G.t, (uint32_t)w));
+                    }
+                }
+            }
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
                 const int off = s * NT * 4 + tid * 4;
@@ -353,22 +377,9 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                     g[2] = __uint_as_float(v.y << 16);
                     g[3] = __uint_as_float(v.y & 0xFFFF0000u);
                 } else {
-                    g[0] = g[1] = g[2] = g[3] = 0.0f;
-                    if (nv[s] > 0) {
-                        if (heavy[s] != 0xFu) {
-                            float zz[4];
-                            gen::grads_normal4(G.seed, (uint64_t)(base + off) >> 2, G.t, (uint32_t)w, zz);
+                    // elements past N draw values too; they are masked below
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) g[c] = fmul(stdv[s][c], zz[c]);
-                        }
-                        if (heavy[s]) {
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                if ((heavy[s] >> c) & 1u)
-                                    g[c] = fmul(G.heavy_scale,
-                                                gen::student_t3(G.seed, base + off + c, G.t, (uint32_t)w));
-                        }
-                    }
+                    for (int c = 0; c < 4; ++c) g[c] = gin[s][c];
                 }
                 const float4 e = *reinterpret_cast<const float4*>(eb + off);
                 const float ee[4] = {e.x, e.y, e.z, e.w};
