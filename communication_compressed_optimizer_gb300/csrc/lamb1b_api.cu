@@ -224,7 +224,6 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     P.fmin = hp->factor_min; P.fmax = hp->factor_max;
     P.fthr_lo = 1.0f - hp->factor_threshold;
     P.fthr_hi = 1.0f + hp->factor_threshold;
-    P.inv_dummy = 0.0f;
     P.check_finite = hp->check_finite;
     P.adam = hp->variant == 1 ? 1 : 0;
 

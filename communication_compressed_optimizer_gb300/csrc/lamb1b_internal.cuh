@@ -23,7 +23,6 @@ struct Problem {
     float omega1, omega2;             // fl(1 - beta1), fl(1 - beta2)
     float cmin, cmax, cema, one_m_cema;
     float fmin, fmax, fthr_lo, fthr_hi; // fl(1 - thr), fl(1 + thr)
-    float inv_dummy;
     int32_t check_finite;
     int32_t adam;       // 1-bit Adam variant: no layerwise coefficient, no fresh variance
 };
@@ -92,55 +91,6 @@ __device__ __forceinline__ float warp_tree128(float f0, float f1, float f2, floa
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
-}
-
-// Pairwise tree over `n` consecutive 128-leaf partials red[0..n) (n a power
-// of two); every lane of the calling warp returns the total.  Partials past
-// n are +0, which leaves the tree's value unchanged.
-template <int NPART>
-__device__ __forceinline__ float tree_over_partials(const float* red, int lane)
-{
-    float v;
-    if constexpr (NPART <= 32) {
-        v = (lane < NPART) ? red[lane] : 0.0f;
-    } else {
-        constexpr int PER = NPART / 32;
-        float t[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) t[j] = red[lane * PER + j];
-#pragma unroll
-        for (int w = 1; w < PER; w <<= 1)
-#pragma unroll
-            for (int j = 0; j < PER; j += 2 * w) t[j] = fadd(t[j], t[j + w]);
-        v = t[0];
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
-
-// Places bit k of the low byte of x at bit 4k.
-__device__ __forceinline__ uint32_t spread8(uint32_t x)
-{
-    x &= 0xFFu;
-    x = (x | (x << 12)) & 0x000F000Fu;
-    x = (x | (x << 6)) & 0x03030303u;
-    x = (x | (x << 3)) & 0x11111111u;
-    return x;
-}
-
-// The warp holds 128 consecutive elements, 4 per lane; p0..p3 are the sign
-// predicates of the lane's components.  Lanes 0..3 return sign word `lane`
-// of the block (element 32*lane + b at bit b); other lanes return 0.
-__device__ __forceinline__ uint32_t pack_signs128(bool p0, bool p1, bool p2, bool p3, int lane)
-{
-    const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, p0);
-    const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, p1);
-    const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, p2);
-    const uint32_t b3 = __ballot_sync(0xFFFFFFFFu, p3);
-    const int sh = 8 * (lane & 3);
-    return spread8(b0 >> sh) | (spread8(b1 >> sh) << 1) | (spread8(b2 >> sh) << 2) |
-           (spread8(b3 >> sh) << 3);
 }
 
 // ---- launchers (one translation unit each) ---------------------------------

@@ -170,3 +170,31 @@ def test_call_order_and_argument_errors():
     rc = L.lamb1b_init(ctypes.byref(ctx), arr, len(arr), ctypes.byref(h), ctypes.c_void_p(hp_ptr),
                        ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
     assert rc == _abi.ERR_ARG and ctx.value is None
+
+
+def test_trace_events_time_every_kernel_of_a_step():
+    """lamb1b_set_trace_events: four events around the three kernels of a
+    step, recorded on the step's stream; then tracing off again."""
+    wl = _bert_mini()
+    x = torch.from_numpy(workload.gen_params(wl)).cuda()
+    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    ld = grad_ld(wl)
+    stream = torch.cuda.Stream()
+    for stage in ("warmup", "compress"):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        opt.set_trace_events(ev)
+        g = device_grads(wl, 0 if stage == "warmup" else 2, ld)
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            if stage == "warmup":
+                opt.warmup_step(g, stream=stream)
+            else:
+                opt.compress_step(g, stream=stream)
+        stream.synchronize()
+        times = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+        assert all(t >= 0 for t in times) and ev[0].elapsed_time(ev[3]) > 0
+        opt.set_trace_events(None)
+        if stage == "warmup":
+            opt.freeze_variance(stream=stream)
+    with pytest.raises(pkg.Lamb1bError):
+        _abi.check("lamb1b_set_trace_events", _abi.load().lamb1b_set_trace_events(opt._ctx, None, 4))
