@@ -45,6 +45,8 @@ def parse_args():
                    choices=("tiny", "base", "large", "large_w32", "gpt2xl"))
     p.add_argument("--variant", choices=("lamb", "adam"), default="lamb",
                    help="1-bit LAMB (default) or the 1-bit Adam variant")
+    p.add_argument("--errors", choices=("f32", "bf16"), default="f32",
+                   help="storage of the worker and server error buffers")
     p.add_argument("--max-params", type=int, default=0,
                    help="keep only the leading tensors up to this many parameters (profiling)")
     p.add_argument("--warmup-stage-steps", type=int, default=-1,
@@ -75,14 +77,16 @@ def grad_bytes(wl):
     return {"f32": 4, "bf16": 2, "philox": 0}[wl.grad]
 
 
-def fused_kernel_bytes(wl, variant="lamb"):
+def fused_kernel_bytes(wl, variant="lamb", errors="f32"):
     """Algorithmic HBM bytes of one launch of the fused compression kernel:
     per parameter W*(g + 4 e_w read + 4 e_w written + 1/8 signs) + reads of
     4 m + 4 e_s + 4 v + 4 v_fresh and writes of 4 e_s + 4 m + 4 v_fresh +
     1/8 server signs; plus 4 bytes per written scale (W worker + 1 server)."""
     W = wl.W
-    # 1-bit Adam reads and writes no second moments in this kernel
-    per = W * (grad_bytes(wl) + 8.125) + (16.125 if variant == "adam" else 28.125)
+    # 1-bit Adam reads and writes no second moments in this kernel; bfloat16
+    # error storage moves 2 + 2 instead of 4 + 4 bytes per error element
+    eb = 4.0 if errors == "bf16" else 8.0
+    per = W * (grad_bytes(wl) + eb + 0.125) + (eb + 8.125 + (0.0 if variant == "adam" else 12.0))
     return wl.N * per + 4.0 * wl.K * (W + 1)
 
 
@@ -91,8 +95,8 @@ def update_kernel_bytes(wl):
     return wl.N * 12.125 + 4.0 * wl.K
 
 
-def step_bytes(wl, variant="lamb"):
-    return fused_kernel_bytes(wl, variant) + update_kernel_bytes(wl)
+def step_bytes(wl, variant="lamb", errors="f32"):
+    return fused_kernel_bytes(wl, variant, errors) + update_kernel_bytes(wl)
 
 
 def measured_peaks():
@@ -107,7 +111,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha1()
-    for f in ("k_compress.cu", "lamb1b_internal.cuh"):
+    for f in ("k_compress.cuh", "k_compress.cu", "lamb1b_internal.cuh"):
         with open(os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -338,7 +342,8 @@ def run_ours(args, world, rank, local):
 
     x = torch.empty(N, device="cuda")
     pkg.gen_params(x, 0, N, wl.param_std, wl.seed)
-    opt = pkg.OneBitLamb(x, layers, W, C, **dict(wl.hp, variant=args.variant))
+    opt = pkg.OneBitLamb(x, layers, W, C, **dict(wl.hp, variant=args.variant,
+                                                 error_storage=args.errors))
     if wl.grad == "philox":
         g = pkg.PhiloxGrads(wl.seed, wl.layer_std, wl.layer_heavy, wl.heavy_scale)
 
@@ -403,7 +408,7 @@ def run_ours(args, world, rank, local):
     ms_per_step = 1e3 * total_s / args.steps
 
     peak, peak_kind = measured_peaks()
-    kb = fused_kernel_bytes(wl, args.variant)
+    kb = fused_kernel_bytes(wl, args.variant, args.errors)
     k_avg = statistics.mean(kern_ms)
     achieved = kb / (k_avg / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
@@ -453,13 +458,14 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": wl.name, "W": W, "chunk": C, "params": N, "tensors": wl.L,
                    "grads": wl.grad, "variant": f"1-bit {args.variant.upper() if args.variant == 'lamb' else 'Adam'}",
+                   "error_storage": args.errors,
                    "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each step moves %.1f GB); gradients regenerated "
-                         "on the device between timed steps" % (step_bytes(wl, args.variant) / 1e9),
+                         "on the device between timed steps" % (step_bytes(wl, args.variant, args.errors) / 1e9),
                    "timing": "CUDA events on the launching stream around each step"},
         "roofline": roofline,
-        "step": {"alg_bytes": step_bytes(wl, args.variant), "hbm_gbs": step_bytes(wl, args.variant) / (ms_per_step / 1e3) / 1e9,
-                 "frac_of_peak": step_bytes(wl, args.variant) / (ms_per_step / 1e3) / 1e9 / peak,
+        "step": {"alg_bytes": step_bytes(wl, args.variant, args.errors), "hbm_gbs": step_bytes(wl, args.variant, args.errors) / (ms_per_step / 1e3) / 1e9,
+                 "frac_of_peak": step_bytes(wl, args.variant, args.errors) / (ms_per_step / 1e3) / 1e9 / peak,
                  "kernel_ms": {"compress": k_avg, "factor": statistics.mean(factor_ms),
                                "update": statistics.mean(upd_ms)},
                  "ms_p10": float(np.percentile(step_ms, 10)),

@@ -46,6 +46,8 @@ def _hparams(W, chunk, hp):
         setattr(h, k, float(hp[k]))
     h.check_finite = int(hp.get("check_finite", 0))
     h.variant = {"lamb": 0, "adam": 1}.get(hp.get("variant", 0), hp.get("variant", 0))
+    h.error_storage = {"f32": 0, "bf16": 1}.get(hp.get("error_storage", 0),
+                                                hp.get("error_storage", 0))
     return h
 
 
@@ -190,15 +192,16 @@ class OneBitLamb:
 
         def view(ptr, n, dtype, shape=None):
             off = ptr - base
-            nbytes = n * 4
+            nbytes = n * torch.empty((), dtype=dtype).element_size()
             t = self.workspace[off:off + nbytes].view(dtype)
             return t if shape is None else t.view(*shape)
 
         Np, K, WL, L, W = s.Np, s.K, s.words_ld, s.L, s.W
         f32, i32 = torch.float32, torch.int32
+        et = torch.bfloat16 if self._h.error_storage == 1 else f32   # error buffers
         out = dict(
             m=view(s.m, Np, f32), v=view(s.v, Np, f32), v_fresh=view(s.v_fresh, Np, f32),
-            e_s=view(s.e_s, Np, f32), e_w=view(s.e_w, W * Np, f32, (W, Np)),
+            e_s=view(s.e_s, Np, et), e_w=view(s.e_w, W * Np, et, (W, Np)),
             signs_w=view(s.signs_w, W * WL, i32, (W, WL)), signs_s=view(s.signs_s, WL, i32),
             scale_w=view(s.scale_w, W * K, f32, (W, K)), scale_s=view(s.scale_s, K, f32),
             c_bar=view(s.c_bar, L, f32), r_prev=view(s.r_prev, L, f32),

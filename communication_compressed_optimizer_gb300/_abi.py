@@ -37,7 +37,7 @@ class HParams(ctypes.Structure):
                 ("coeff_ema", ctypes.c_float),
                 ("factor_min", ctypes.c_float), ("factor_max", ctypes.c_float),
                 ("factor_threshold", ctypes.c_float), ("check_finite", ctypes.c_int32),
-                ("variant", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("error_storage", ctypes.c_int32)]
 
 
 class GradsDesc(ctypes.Structure):

@@ -14,7 +14,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblamb1b.so")
 
-SOURCES = ["lamb1b_api.cu", "k_compress.cu", "k_lamb.cu", "gen.cu", "noalloc.cu"]
+SOURCES = ["lamb1b_api.cu", "k_compress.cu", "k_compress_lamb_f32.cu", "k_compress_lamb_bf16.cu",
+           "k_compress_adam_f32.cu", "k_compress_adam_bf16.cu", "k_lamb.cu", "gen.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
               "-ffp-contract=off", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -1,547 +1,9 @@
-// Compression stage of 1-bit LAMB (arXiv 2104.06069): the fused worker +
-// server pass and the per-tensor factor.
-//
-// One CTA owns a tile of whole chunks for all W virtual workers, so the
-// "communication" of the compressed allreduce (section 5 summary: gather chunk
-// k of every worker at server k, average, scatter the average) happens in
-// registers: the worker loop accumulates each element's server sum while the
-// worker's sign bits are still live, and the packed words and scales are also
-// written to the exchange buffers (signs_w, scale_w) as the message.
-//
-// Data movement: CTAs are persistent (tile t = blockIdx.x + i*gridDim.x; a
-// tile is 4096 elements = 4096/C chunks, or one 8192-element chunk).
-// Every input of a tile -- the old momentum, each worker's gradient and
-// error, then the server error, frozen and fresh second moments -- is copied
-// into a 7-slot ring of shared-memory slots by TMA bulk copies
-// (cp.async.bulk, completion on one mbarrier per slot), issued by thread 0 as
-// soon as enough slots are released, so the next arrays stream in while the
-// CTA reduces and stores the current one; while the server phase holds its
-// three arrays the next tile's momentum and first worker are already loading.  Outputs are written with coalesced 16-byte stores.
-//
-// Thread map: thread `tid` of an NT-thread CTA holds SLOTS aligned float4
-// groups, group s at chunk offset s*NT*4 + tid*4.  Warp w's lanes therefore
-// cover the 128 consecutive elements starting at s*NT*4 + w*128, which is one
-// leaf block of the canonical pairwise tree.
-#include "lamb1b_internal.cuh"
+// Compression stage of 1-bit LAMB (arXiv 2104.06069): dispatch of the fused
+// worker + server pass (k_compress.cuh, one translation unit per variant and
+// error storage), the per-tensor factor kernel and the update.
+#include "k_compress.cuh"
 
 namespace lamb1b {
-
-// ---- TMA bulk copies and mbarriers (inline PTX, sm_90+) ----------------------
-namespace tma {
-
-__device__ __forceinline__ uint32_t saddr(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count) : "memory");
-}
-
-// makes the initialised barriers visible to the asynchronous (TMA) proxy
-__device__ __forceinline__ void fence_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void arrive_expect_tx(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned
-__device__ __forceinline__ void load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(saddr(dst)), "l"(src), "r"(bytes), "r"(saddr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ bool try_wait(uint64_t* bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(saddr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-}  // namespace tma
-
-// Bounded wait for a stage: try_wait suspends for a hardware-defined time per
-// call, so this gives up after seconds, never hangs.
-constexpr uint32_t kMaxWaitTries = 1u << 24;
-
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity)
-{
-    for (uint32_t it = 0; it < kMaxWaitTries; ++it)
-        if (tma::try_wait(bar, parity)) return true;
-    return false;
-}
-
-// Word r of a warp's 128-element block: lanes 8r..8r+7 each hold a nibble of
-// 4 consecutive sign bits; OR-combine them across the 8 lanes.  Every lane of
-// the group returns the word.
-__device__ __forceinline__ uint32_t pack_nibbles(uint32_t nib, int lane)
-{
-    uint32_t v = nib << (4 * (lane & 7));
-    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    return v;
-}
-
-template <int GK>
-struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGradBF16 ? 2 : 0); };
-
-// Ring of NSLOT shared-memory slots of TILE floats, one mbarrier per slot.
-// Every tile streams, in slot positions: M (m_old), then per worker W_w its
-// gradients (when stored) and its error, then S (e_s, and v for 1-bit LAMB),
-// then F (v_fresh, 1-bit LAMB only).  Slot position p lives in slot p % NSLOT
-// and completes phase (p / NSLOT) of that slot's barrier.
-template <int TILE>
-struct Ring {
-    static constexpr uint32_t kSlot = TILE * 4;
-};
-
-template <int SG, bool ADAM>
-struct Stream {
-    static constexpr int kPerWorker = SG > 0 ? 2 : 1;
-    static constexpr int kServer = ADAM ? 1 : 2;         // slots of item S
-    __device__ static int items(int W) { return W + (ADAM ? 2 : 3); }
-    // slots of item r
-    __device__ static int slots(int r, int W) { return r == 0 ? 1 : (r <= W ? kPerWorker : (r == W + 1 ? kServer : 1)); }
-};
-
-// A slot position kept as (slot, barrier phase), advanced without division.
-template <int NSLOT>
-struct RingPos {
-    int slot = 0;
-    uint32_t phase = 0;
-    __device__ __forceinline__ RingPos plus(int n) const
-    {
-        RingPos q = *this;
-        q.slot += n;
-        if (q.slot >= NSLOT) { q.slot -= NSLOT; q.phase ^= 1u; }
-        return q;
-    }
-};
-
-// Producer side: issue the bulk copies of item r of tile t whose first slot
-// position is p; called by thread 0 only.
-template <int TILE, int SG, int NSLOT, bool ADAM>
-__device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, const Problem& P,
-                                           const Dev& D, const Grads& G, unsigned char* ring,
-                                           uint64_t* full)
-{
-    using R = Ring<TILE>;
-    const int W = P.W;
-    const int64_t base = t * TILE;
-    auto copy = [&](int k, const void* src, uint32_t bytes) {
-        const int sl = p.plus(k).slot;
-        tma::arrive_expect_tx(&full[sl], bytes);
-        tma::load(ring + (uint32_t)sl * R::kSlot, src, bytes, &full[sl]);
-    };
-    if (r == 0) {
-        copy(0, D.m + base, R::kSlot);
-    } else if (r <= W) {
-        const int w = r - 1;
-        if constexpr (SG > 0) {
-            const int64_t n_t = (base + TILE <= P.N) ? (int64_t)TILE : P.N - base;
-            const uint32_t gbytes = (uint32_t)(((n_t * SG) + 15) / 16 * 16);
-            copy(0, static_cast<const unsigned char*>(G.ptr) + ((int64_t)w * G.ld + base) * SG, gbytes);
-            copy(1, D.e_w + (int64_t)w * P.Np + base, R::kSlot);
-        } else {
-            copy(0, D.e_w + (int64_t)w * P.Np + base, R::kSlot);
-        }
-    } else if (r == W + 1) {
-        copy(0, D.e_s + base, R::kSlot);
-        if constexpr (!ADAM) copy(1, D.v + base, R::kSlot);
-    } else {
-        copy(0, D.v_fresh + base, R::kSlot);
-    }
-}
-
-// Consumer side: wait for n consecutive slots starting at p.
-template <int NSLOT>
-__device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int n)
-{
-    bool ok = true;
-    for (int k = 0; k < n; ++k) {
-        const RingPos<NSLOT> q = p.plus(k);
-        ok &= wait_stage(&full[q.slot], q.phase);
-    }
-    return ok;
-}
-
-// Chunk totals from the tile's 128-leaf partials red[0 .. NPART) (element
-// order).  Lane j returns the canonical sum of squares of chunk j / LPC of
-// the tile, LPC = lanes per chunk: the first log2(LPC) butterfly stages are
-// exactly the pairwise tree over each chunk's partials.
-template <int NPART, int PPC>
-__device__ __forceinline__ float chunk_totals(const float* red, int lane)
-{
-    constexpr int PER = NPART > 32 ? NPART / 32 : 1;
-    constexpr int LPC = PPC / PER;
-    static_assert(PPC % PER == 0 && LPC >= 1 && LPC <= 32, "chunk / tile shape");
-    float v;
-    if constexpr (PER == 1) {
-        v = (lane < NPART) ? red[lane] : 0.0f;
-    } else {
-        float t[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) t[j] = red[lane * PER + j];
-#pragma unroll
-        for (int w = 1; w < PER; w <<= 1)
-#pragma unroll
-            for (int j = 0; j < PER; j += 2 * w) t[j] = fadd(t[j], t[j + w]);
-        v = t[0];
-    }
-#pragma unroll
-    for (int o = 1; o < LPC; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
-
-// Two CTAs per SM when two rings fit in shared memory, else one.
-template <int NT, int SLOTS, int NSLOT>
-struct MinBlocks {
-    static constexpr int value = (NSLOT * (NT * 4 * SLOTS) * 4 <= 112 * 1024) ? 2 : 1;
-};
-
-template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM>
-__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
-    k_compress(const Problem P, const Dev D, const Grads G)
-{
-    constexpr int NWARP = NT / 32;
-    constexpr int TILE = NT * 4 * SLOTS;
-    constexpr int NPART = TILE / 128;           // 128-leaf partials per tile
-    constexpr int PPC = C / 128;                // partials per chunk
-    constexpr int PER = NPART > 32 ? NPART / 32 : 1;
-    constexpr int LPC = PPC / PER;              // lanes per chunk in chunk_totals
-    constexpr int CPT = TILE / C;               // chunks per tile
-    constexpr int SG = GradBytes<GK>::value;
-    static_assert(TILE % C == 0, "a tile holds whole chunks");
-    using R = Ring<TILE>;
-    using SL = Stream<SG, ADAM>;
-    extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ uint64_t full[NSLOT];
-    __shared__ float red[2][NPART];
-    __shared__ uint32_t lmax[kMaxChunkLayers];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int W = P.W;
-    const int TPC = SL::items(W);                       // stream items per tile
-    const int64_t ntiles = P.Np / TILE;
-    const int64_t nloc = (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
-
-    if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) tma::bar_init(&full[s], 1);
-        tma::fence_init();
-    }
-    for (int i = tid; i < kMaxChunkLayers; i += NT) lmax[i] = 0u;
-    __syncthreads();
-
-    // ---- producer (thread 0): items in order, as long as all their slots
-    // fit in the ring ahead of the released slot positions ------------------
-    int issue_pos = 0, released = 0;          // slot positions (per CTA)
-    int64_t issue_tile = 0;                   // local tile index of the next item
-    int issue_r = 0;                          // its kind
-    RingPos<NSLOT> ip;                        // its first slot
-    auto issue_ready = [&]() {
-        while (issue_tile < nloc) {
-            const int n = SL::slots(issue_r, W);
-            if (issue_pos + n > released + NSLOT) break;
-            issue_item<TILE, SG, NSLOT, ADAM>(blockIdx.x + issue_tile * gridDim.x, issue_r, ip,
-                                              P, D, G, ring, full);
-            issue_pos += n;
-            ip = ip.plus(n);
-            if (++issue_r == TPC) { issue_r = 0; ++issue_tile; }
-        }
-    };
-    if (tid == 0) issue_ready();
-    RingPos<NSLOT> cp;                        // consumer: next slot to read
-
-    bool bad = false;        // non-finite gradient seen
-    bool lost = false;       // a stage wait gave up
-
-    for (int64_t ti = 0; ti < nloc; ++ti) {
-        const int64_t tile = blockIdx.x + ti * gridDim.x;
-        const int64_t base = tile * TILE;
-        const bool full_tile = base + TILE <= P.N;
-        const int64_t k0 = base / C;                     // first chunk of the tile
-        const int64_t klast = (k0 + CPT - 1 < P.K - 1) ? k0 + CPT - 1 : P.K - 1;
-        const int l0 = D.chunk_l0[k0];
-        // this lane's chunk in chunk_totals, and its element count
-        const int64_t kq = k0 + lane / LPC;
-        const int64_t nq_raw = P.N - kq * C;
-        const float nq = (float)(nq_raw >= C ? C : (nq_raw > 0 ? nq_raw : 0));
-        const bool lane_stores_scale = (lane % LPC) == 0 && lane / LPC < CPT && kq < P.K;
-
-        int nv[SLOTS];
-        int qsrc[SLOTS];       // lane holding the scale of this slot's chunk
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            const int64_t r = P.N - (base + s * NT * 4 + tid * 4);
-            nv[s] = r >= 4 ? 4 : (r > 0 ? (int)r : 0);
-            qsrc[s] = ((s * NT * 4 + warp * 128) / C) * LPC;
-        }
-
-        // in-kernel gradients: per-element std and Student-t flags
-        float stdv[SLOTS][4];
-        uint32_t heavy[SLOTS];
-        if constexpr (GK == kGradPhilox) {
-            int l = l0;
-            int64_t lend = D.layer_end[l];
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                heavy[s] = 0u;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    stdv[s][c] = 0.0f;
-                    if (c < nv[s]) {
-                        const int64_t i = base + s * NT * 4 + tid * 4 + c;
-                        while (i >= lend) { ++l; lend = D.layer_end[l]; }
-                        stdv[s][c] = G.layer_std[l];
-                        if (G.layer_heavy && G.layer_heavy[l]) heavy[s] |= 1u << c;
-                    }
-                }
-            }
-        }
-
-        // ---- item M: beta1 * m_old, kept for the whole tile ------------------
-        float bm[SLOTS][4], acc[SLOTS][4];
-        {
-            if (!wait_slots<NSLOT>(full, cp, 1)) lost = true;
-            const float* a = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
-            cp = cp.plus(1);
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const float4 mo = *reinterpret_cast<const float4*>(a + s * NT * 4 + tid * 4);
-                bm[s][0] = fmul(P.beta1, mo.x); bm[s][1] = fmul(P.beta1, mo.y);
-                bm[s][2] = fmul(P.beta1, mo.z); bm[s][3] = fmul(P.beta1, mo.w);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[s][c] = 0.0f;
-            }
-        }
-
-        // ---- phase 1: every worker compresses its chunks ----------------------
-        for (int w = 0; w < W; ++w) {
-            if (!wait_slots<NSLOT>(full, cp, SL::kPerWorker)) lost = true;
-            const unsigned char* a = ring + (uint32_t)cp.slot * R::kSlot;
-            const float* eb = reinterpret_cast<const float*>(
-                ring + (uint32_t)cp.plus(SL::kPerWorker - 1).slot * R::kSlot);
-            cp = cp.plus(SL::kPerWorker);
-            float z[SLOTS][4];
-            // in-kernel gradients: the normal draws of all slots first, as
-            // independent Philox chains (instruction-level parallelism), then
-            // the Student-t draws of the heavy-tailed tensors' elements
-            float gin[SLOTS][4];
-            if constexpr (GK == kGradPhilox) {
-#pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    gen::grads_normal4(G.seed, (uint64_t)(base + s * NT * 4 + tid * 4) >> 2, G.t,
-                                       (uint32_t)w, gin[s]);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) gin[s][c] = fmul(stdv[s][c], gin[s][c]);
-                }
-#pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    if (heavy[s]) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if ((heavy[s] >> c) & 1u)
-                                gin[s][c] = fmul(G.heavy_scale,
-                                                 gen::student_t3(G.seed, base + s * NT * 4 + tid * 4 + c,
-                                                                 G.t, (uint32_t)w));
-                    }
-                }
-            }
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                float g[4];
-                if constexpr (GK == kGradF32) {
-                    const float4 v = *reinterpret_cast<const float4*>(a + off * 4);
-                    g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
-                } else if constexpr (GK == kGradBF16) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(a + off * 2);
-                    g[0] = __uint_as_float(v.x << 16);
-                    g[1] = __uint_as_float(v.x & 0xFFFF0000u);
-                    g[2] = __uint_as_float(v.y << 16);
-                    g[3] = __uint_as_float(v.y & 0xFFFF0000u);
-                } else {
-                    // elements past N draw values too; they are masked below
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) g[c] = gin[s][c];
-                }
-                const float4 e = *reinterpret_cast<const float4*>(eb + off);
-                const float ee[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_tile || c < nv[s];
-                    if (P.check_finite && valid && !isfinite(g[c])) bad = true;
-                    const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
-                    z[s][c] = valid ? fadd(mw, ee[c]) : 0.0f;
-                }
-                const float t = warp_tree128(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1]),
-                                             fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3]));
-                if (lane == 0) red[w & 1][s * NWARP + warp] = t;
-            }
-            if (__syncthreads_or(lost)) goto abort;
-            released += (w == 0) ? 1 + SL::kPerWorker : SL::kPerWorker;
-            if (tid == 0) issue_ready();
-            const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
-            const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
-            uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld;
-            float* ew = D.e_w + (int64_t)w * P.Np;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                const float sc = (CPT == 1) ? sq : __shfl_sync(0xFFFFFFFFu, sq, qsrc[s]);
-                uint32_t nib = 0u;
-                float en[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_tile || c < nv[s];
-                    const bool pos = !(z[s][c] < 0.0f);
-                    const float ss = pos ? sc : -sc;
-                    nib |= (valid && pos) ? (1u << c) : 0u;
-                    en[c] = valid ? fsub(z[s][c], ss) : 0.0f;
-                    acc[s][c] = fadd(acc[s][c], ss);
-                }
-                const uint32_t word = pack_nibbles(nib, lane);
-                if ((lane & 7) == 0)
-                    sw[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
-                *reinterpret_cast<float4*>(ew + base + off) = make_float4(en[0], en[1], en[2], en[3]);
-            }
-            if (warp == 0 && lane_stores_scale) D.scale_w[(int64_t)w * P.K + kq] = sq;
-        }
-
-        // ---- phases 2 and 3: server average, recompression, scatter ----------
-        {
-            const int nsrv = SL::kServer + (ADAM ? 0 : 1);      // S (and F) slots
-            if (!wait_slots<NSLOT>(full, cp, nsrv)) lost = true;
-            const float* es_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
-            const float* v_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(1).slot * R::kSlot);
-            const float* vf_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(2).slot * R::kSlot);
-            cp = cp.plus(nsrv);
-            float y[SLOTS][4], vz[SLOTS][4], vfo[SLOTS][4];
-            const float Wf = (float)W;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                const float4 e = *reinterpret_cast<const float4*>(es_in + off);
-                const float ee[4] = {e.x, e.y, e.z, e.w};
-                if constexpr (!ADAM) {
-                    const float4 v = *reinterpret_cast<const float4*>(v_in + off);
-                    const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
-                    vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
-                    vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_tile || c < nv[s];
-                    y[s][c] = valid ? fadd(fdiv(acc[s][c], Wf), ee[c]) : 0.0f;
-                }
-                const float t = warp_tree128(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1]),
-                                             fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3]));
-                if (lane == 0) red[W & 1][s * NWARP + warp] = t;
-            }
-            if (__syncthreads_or(lost)) goto abort;
-            released += nsrv;
-            if (tid == 0) issue_ready();
-            const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
-            const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
-
-            int l = l0;
-            int64_t lend = D.layer_end[l];
-            int lcur = -1;
-            uint32_t runmax = 0u;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                const float ss = (CPT == 1) ? ssq : __shfl_sync(0xFFFFFFFFu, ssq, qsrc[s]);
-                uint32_t nib = 0u;
-                float es[4], mn[4], vf[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_tile || c < nv[s];
-                    const bool pos = !(y[s][c] < 0.0f);
-                    const float sgn = pos ? ss : -ss;
-                    nib |= (valid && pos) ? (1u << c) : 0u;
-                    es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
-                    mn[c] = valid ? sgn : 0.0f;
-                    if constexpr (ADAM) continue;
-                    // reconstructed gradient and fresh second moment
-                    const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
-                    vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
-                    if (valid) {
-                        float rho = fdiv(fadd(fsqrt(vz[s][c]), P.eps), fadd(fsqrt(vf[c]), P.eps));
-                        if (rho != rho) rho = __int_as_float(0x7F800000);
-                        const int64_t i = base + off + c;
-                        while (i >= lend) { ++l; lend = D.layer_end[l]; }
-                        if (l != lcur) {
-                            if (lcur >= 0) {
-                                if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
-                                else atomicMax(&D.Rmax[lcur], runmax);
-                            }
-                            lcur = l;
-                            runmax = 0u;
-                        }
-                        runmax = max(runmax, __float_as_uint(rho));
-                    }
-                }
-                const uint32_t word = pack_nibbles(nib, lane);
-                if ((lane & 7) == 0)
-                    D.signs_s[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
-                *reinterpret_cast<float4*>(D.e_s + base + off) = make_float4(es[0], es[1], es[2], es[3]);
-                *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-                if constexpr (!ADAM)
-                    *reinterpret_cast<float4*>(D.v_fresh + base + off) =
-                        make_float4(vf[0], vf[1], vf[2], vf[3]);
-            }
-            if (lcur >= 0) {
-                if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
-                else atomicMax(&D.Rmax[lcur], runmax);
-            }
-            if (warp == 0 && lane_stores_scale) D.scale_s[kq] = ssq;
-        }
-        __syncthreads();
-        {
-            const int nl = D.chunk_l1[klast] - l0 + 1;
-            for (int jj = tid; jj < nl && jj < kMaxChunkLayers; jj += NT) {
-                const uint32_t v = lmax[jj];
-                lmax[jj] = 0u;
-                if (v) atomicMax(&D.Rmax[l0 + jj], v);
-            }
-        }
-    }
-    if (bad) atomicOr(D.flags, 1u);
-    return;
-
-abort:
-    // A stage wait gave up (never expected).  Record it, let the copies this
-    // CTA still has in flight land (bounded), then leave.
-    if (tid == 0) {
-        atomicOr(D.flags, 2u);
-        // every slot position issued but not yet released (at most NSLOT):
-        // they end at the producer's position ip
-        RingPos<NSLOT> q = ip;
-        for (int k = issue_pos - released; k > 0; --k) {
-            q.slot -= 1;
-            if (q.slot < 0) { q.slot += NSLOT; q.phase ^= 1u; }
-            wait_stage(&full[q.slot], q.phase);
-        }
-    }
-    __syncthreads();
-}
 
 // Per tensor: soft-thresholded factor from the max ratio, coefficient, and
 // reset of the max for the next step.
@@ -560,55 +22,6 @@ __global__ void k_factor(const Problem P, const Dev D)
     D.gc[l] = fmul(P.lr, c);
 }
 
-cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st);
-
-template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM>
-static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
-{
-    constexpr int TILE = NT * 4 * SLOTS;
-    constexpr size_t smem = (size_t)NSLOT * Ring<TILE>::kSlot;
-    auto kern = k_compress<NT, SLOTS, GK, NSLOT, C, ADAM>;
-    // per-device launch shape, computed once per instantiation
-    static int cached_device = -1;
-    static int grid_cap = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (cached_device != dev) {
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                      cudaSharedmemCarveoutMaxShared)))
-            return e;
-        int per_sm = 0, sms = 0;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem))) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
-        grid_cap = (per_sm > 0 ? per_sm : 1) * sms;
-        cached_device = dev;
-    }
-    const int64_t ntiles = P.Np / TILE;
-    const unsigned grid = (unsigned)(ntiles < grid_cap ? ntiles : grid_cap);
-    kern<<<grid, NT, smem, st>>>(P, D, G);
-    return cudaGetLastError();
-}
-
-template <int NT, int SLOTS, int NSLOT, int C, bool ADAM>
-static cudaError_t launch_grad(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
-{
-    switch (G.kind) {
-    case kGradF32:  return launch_one<NT, SLOTS, kGradF32, NSLOT, C, ADAM>(P, D, G, st);
-    case kGradBF16: return launch_one<NT, SLOTS, kGradBF16, NSLOT, C, ADAM>(P, D, G, st);
-    default:        return launch_one<NT, SLOTS, kGradPhilox, NSLOT, C, ADAM>(P, D, G, st);
-    }
-}
-
-template <int NT, int SLOTS, int NSLOT, int C>
-static cudaError_t launch_kind(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
-{
-    return P.adam ? launch_grad<NT, SLOTS, NSLOT, C, true>(P, D, G, st)
-                  : launch_grad<NT, SLOTS, NSLOT, C, false>(P, D, G, st);
-}
-
 int64_t padded_length(int64_t N, int C)
 {
     const int64_t tile = C > 4096 ? C : 4096;
@@ -622,15 +35,10 @@ cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, floa
     if ((e = trace(ev, 0, st)) != cudaSuccess) return e;
     // 4096-element tiles (256 threads x 4 float4 groups) holding 4096/C chunks;
     // 8192-element chunks use 512-thread tiles of one chunk.
-    switch (P.C) {
-    case 256:  e = launch_kind<256, 4, 7, 256>(P, D, G, st); break;
-    case 512:  e = launch_kind<256, 4, 7, 512>(P, D, G, st); break;
-    case 1024: e = launch_kind<256, 4, 7, 1024>(P, D, G, st); break;
-    case 2048: e = launch_kind<256, 4, 7, 2048>(P, D, G, st); break;
-    case 4096: e = launch_kind<256, 4, 7, 4096>(P, D, G, st); break;
-    case 8192: e = launch_kind<512, 4, 7, 8192>(P, D, G, st); break;
-    default:   return cudaErrorInvalidValue;
-    }
+    if (P.adam)
+        e = P.ebf16 ? launch_fused<true, true>(P, D, G, st) : launch_fused<true, false>(P, D, G, st);
+    else
+        e = P.ebf16 ? launch_fused<false, true>(P, D, G, st) : launch_fused<false, false>(P, D, G, st);
     if (e != cudaSuccess) return e;
     if ((e = trace(ev, 1, st)) != cudaSuccess) return e;
     if (!P.adam) {   // 1-bit Adam: c = 1, gc = lr from the initialisation

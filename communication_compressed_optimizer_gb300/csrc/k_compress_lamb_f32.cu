@@ -1,0 +1,13 @@
+// Fused compression kernels for the 1-bit LAMB variant with binary32 error
+// buffers, every chunk size and gradient kind (templates in k_compress.cuh).
+#include "k_compress.cuh"
+
+namespace lamb1b {
+
+template <>
+cudaError_t launch_fused<false, false>(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
+{
+    return launch_fused_all_chunks<false, false>(P, D, G, st);
+}
+
+}  // namespace lamb1b

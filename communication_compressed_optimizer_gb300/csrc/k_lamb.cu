@@ -318,8 +318,9 @@ cudaError_t launch_freeze(const Problem& P, const Dev& D, cudaStream_t st)
     cudaError_t e;
     if ((e = cudaMemcpyAsync(D.v_fresh, D.v, sizeof(float) * P.Np, cudaMemcpyDeviceToDevice, st)))
         return e;
-    if ((e = cudaMemsetAsync(D.e_w, 0, sizeof(float) * P.Np * P.W, st))) return e;
-    if ((e = cudaMemsetAsync(D.e_s, 0, sizeof(float) * P.Np, st))) return e;
+    const size_t fe = P.ebf16 ? 2 : 4;
+    if ((e = cudaMemsetAsync(D.e_w, 0, fe * P.Np * P.W, st))) return e;
+    if ((e = cudaMemsetAsync(D.e_s, 0, fe * P.Np, st))) return e;
     k_layers_reset<<<(P.L + 255) / 256, 256, 0, st>>>(P, D, 0);
     return cudaGetLastError();
 }

@@ -53,6 +53,7 @@ int check_hparams(const lamb1b_hparams* hp)
     if (!(hp->factor_threshold >= 0.0f)) return LAMB1B_ERR_ARG;
     if (hp->check_finite != 0 && hp->check_finite != 1) return LAMB1B_ERR_ARG;
     if (hp->variant != 0 && hp->variant != 1) return LAMB1B_ERR_ARG;
+    if (hp->error_storage != 0 && hp->error_storage != 1) return LAMB1B_ERR_ARG;
     return LAMB1B_OK;
 }
 
@@ -81,8 +82,10 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     p->H = H;
     const size_t f = sizeof(float);
     size_t bytes[R_COUNT];
-    bytes[R_M] = bytes[R_V] = bytes[R_VF] = bytes[R_ES] = f * p->Np;
-    bytes[R_EW] = f * p->Np * p->W;
+    const size_t fe = hp->error_storage ? 2 : 4;   // error element size
+    bytes[R_M] = bytes[R_V] = bytes[R_VF] = f * p->Np;
+    bytes[R_ES] = fe * p->Np;
+    bytes[R_EW] = fe * p->Np * p->W;
     bytes[R_SW] = sizeof(uint32_t) * p->words_ld * p->W;
     bytes[R_SS] = sizeof(uint32_t) * p->words_ld;
     bytes[R_SCW] = f * p->K * p->W;
@@ -226,6 +229,7 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     P.fthr_hi = 1.0f + hp->factor_threshold;
     P.check_finite = hp->check_finite;
     P.adam = hp->variant == 1 ? 1 : 0;
+    P.ebf16 = hp->error_storage == 1 ? 1 : 0;
 
     char* ws = static_cast<char*>(workspace_dev);
     Dev& D = c->D;

@@ -25,6 +25,7 @@ struct Problem {
     float fmin, fmax, fthr_lo, fthr_hi; // fl(1 - thr), fl(1 + thr)
     int32_t check_finite;
     int32_t adam;       // 1-bit Adam variant: no layerwise coefficient, no fresh variance
+    int32_t ebf16;      // e_w and e_s stored as bfloat16
 };
 
 // Device pointers into the caller's workspace.
@@ -32,8 +33,8 @@ struct Dev {
     float* m;         // [Np]
     float* v;         // [Np]  second moment; frozen after the stage switch
     float* v_fresh;   // [Np]
-    float* e_s;       // [Np]
-    float* e_w;       // [W][Np]
+    float* e_s;       // [Np]     binary32, or bfloat16 bits when P.ebf16
+    float* e_w;       // [W][Np]  binary32, or bfloat16 bits when P.ebf16
     uint32_t* signs_w;// [W][words_ld]
     uint32_t* signs_s;// [words_ld]
     float* scale_w;   // [W][K]
@@ -91,6 +92,13 @@ __device__ __forceinline__ float warp_tree128(float f0, float f1, float f2, floa
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
+}
+
+// binary32 -> bfloat16 bits, round to nearest even; NaN -> 0x7FC0
+__device__ __forceinline__ uint32_t bf16_bits(float x)
+{
+    const uint32_t b = __float_as_uint(x);
+    return (x != x) ? 0x7FC0u : ((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);
 }
 
 // ---- launchers (one translation unit each) ---------------------------------

@@ -89,6 +89,14 @@ typedef struct {
                                  the compression stage, no layerwise coefficient
                                  (c = 1), no fresh variance; coeff_* and factor_*
                                  are then unused. */
+    int32_t error_storage;    /* element type of the worker and server error
+                                 buffers (e_w, e_s): 0 binary32; 1 bfloat16,
+                                 rounded to nearest even when stored (NaN is
+                                 stored as 0x7FC0) and widened exactly when
+                                 read.  A storage variant with no counterpart in
+                                 the paper: it halves the largest per-worker
+                                 traffic at the cost of rounding the kept
+                                 compression error to 8 significant bits. */
 } lamb1b_hparams;
 
 typedef enum {
@@ -122,8 +130,9 @@ typedef struct {
  * checkpointing and restore; the caller may read or overwrite them between
  * calls).  Padded layouts: Np = N rounded up to a multiple of max(C, 4096)
  * elements per vector (>= K*C), words_ld = Np/32.
- *   m, v, v_fresh, e_s: [Np] binary32; elements >= N are kept at 0
- *   e_w: [W][Np];   signs_w: [W][words_ld] u32;   signs_s: [words_ld]
+ *   m, v, v_fresh: [Np] binary32; elements >= N are kept at 0
+ *   e_s: [Np], e_w: [W][Np], binary32 or (error_storage = 1) bfloat16 bits
+ *   signs_w: [W][words_ld] u32;   signs_s: [words_ld]
  *   scale_w: [W][K];   scale_s: [K]
  *   c_bar, r_prev, c_cur, R_last, Sx, Su: [L]
  * Sign words: element j at word j/32, bit j%32, bit = 1 for a +1 sign. */
@@ -131,8 +140,8 @@ typedef struct {
     float* m;
     float* v;
     float* v_fresh;
-    float* e_w;
-    float* e_s;
+    void* e_w;          /* element type per lamb1b_hparams.error_storage    */
+    void* e_s;
     uint32_t* signs_w;
     uint32_t* signs_s;
     float* scale_w;

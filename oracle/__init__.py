@@ -49,7 +49,7 @@ class _OrcT(ctypes.Structure):
         ("eps", ctypes.c_float), ("wd", ctypes.c_float),
         ("cmin", ctypes.c_float), ("cmax", ctypes.c_float), ("cema", ctypes.c_float),
         ("fmin", ctypes.c_float), ("fmax", ctypes.c_float), ("fthr", ctypes.c_float),
-        ("pad1", ctypes.c_float),
+        ("err_bf16", ctypes.c_int32),
         ("x", _P), ("m", _P), ("v", _P), ("v_fresh", _P), ("e_w", _P), ("e_s", _P),
         ("signs_w", _P), ("signs_s", _P), ("scale_w", _P), ("scale_s", _P),
         ("c_bar", _P), ("r_prev", _P), ("c_cur", _P), ("R", _P), ("Sx", _P), ("Su", _P),
@@ -70,6 +70,8 @@ def lib():
                                          _P, _P]
         L.orc_compress_chunk.restype = ctypes.c_float
         L.orc_layer_factor.argtypes = [ctypes.c_float] * 5
+        L.orc_bf16_round.argtypes = [ctypes.c_float]
+        L.orc_bf16_round.restype = ctypes.c_float
         L.orc_layer_factor.restype = ctypes.c_float
         for f in ("orc_warmup_step", "orc_compress_step"):
             getattr(L, f).argtypes = [ctypes.POINTER(_OrcT), _P, ctypes.c_int64]
@@ -110,6 +112,10 @@ def compress_chunk(z: np.ndarray, k: int, C: int):
     return np.float32(s), words, err[:n]
 
 
+def bf16_round(x: float) -> np.float32:
+    return np.float32(lib().orc_bf16_round(float(x)))
+
+
 def layer_factor(R, r_prev, fmin, fmax, fthr) -> np.float32:
     return np.float32(lib().orc_layer_factor(R, r_prev, fmin, fmax, fthr))
 
@@ -125,13 +131,14 @@ class Oracle:
                  "c_bar", "r_prev", "c_cur", "R", "Sx", "Su")
 
     def __init__(self, offsets, numels, W: int, chunk: int, hp: dict, x0: np.ndarray,
-                 variant: int = 0):
+                 variant: int = 0, err_bf16: int = 0):
         self.off = np.ascontiguousarray(offsets, dtype=np.int64)
         self.numel = np.ascontiguousarray(numels, dtype=np.int64)
         L = len(self.off)
         N = int(self.numel.sum())
         self.N, self.L, self.W, self.C = N, L, W, chunk
         self.variant = int(variant)
+        self.err_bf16 = int(err_bf16)
         self.K = -(-N // chunk)
         self.NW = -(-N // 32)
         self.hp = dict(hp)
@@ -162,6 +169,7 @@ class Oracle:
         s = _OrcT()
         s.N, s.L, s.W, s.C = self.N, self.L, self.W, self.C
         s.variant = self.variant
+        s.err_bf16 = self.err_bf16
         s.off, s.numel = _p(self.off), _p(self.numel)
         s.lr, s.beta1, s.beta2 = h["lr"], h["beta1"], h["beta2"]
         s.eps, s.wd = h["eps"], h["weight_decay"]

@@ -39,7 +39,9 @@
  *   the warmup coefficients.  Variant 1 is 1-bit Adam (the 1-bit Adam page and
  *   the 1-bit LAMB background on it): vanilla Adam in the warmup, the same
  *   compressed momentum exchange in the compression stage, no layerwise
- *   coefficient and no fresh variance.  Parity with the published algorithm is unpinned
+ *   coefficient and no fresh variance.  err_bf16 = 1 stores the worker and
+ *   server errors rounded to bfloat16 (a storage variant, not in the paper).
+ *   Parity with the published algorithm is unpinned
  *   for those readings (bias correction, clip bounds, scale formula, c_bar,
  *   fresh variance, soft thresholds); the pins here are the stated invariants.
  *
@@ -64,7 +66,8 @@ typedef struct {
     /* hyper-parameters */
     float lr, beta1, beta2, eps, wd;
     float cmin, cmax, cema;
-    float fmin, fmax, fthr, pad1;
+    float fmin, fmax, fthr;
+    int32_t err_bf16;       /* 1: worker and server errors are stored as bf16 */
     /* state, caller-owned */
     float* x;               /* [N] parameters                      */
     float* m;               /* [N] momentum                        */
@@ -105,6 +108,23 @@ static float clip(float x, float a, float b)
     float r = (x < a) ? a : x;
     return (r > b) ? b : r;
 }
+
+/* Round a binary32 value to the nearest bfloat16 (ties to even) and widen it
+ * back; NaN becomes the quiet NaN 0x7FC0.  Storage rounding of the
+ * error-feedback buffers in the bf16 error-storage variant. */
+float orc_bf16_round(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    uint32_t h = (x != x) ? 0x7FC0u : ((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);
+    uint32_t r = h << 16;
+    float y;
+    memcpy(&y, &r, 4);
+    return y;
+}
+
+/* the error buffers keep exactly what the storage format can hold */
+static float store_err(const orc_t* s, float e) { return s->err_bf16 ? orc_bf16_round(e) : e; }
 
 /* ---- canonical pairwise tree ------------------------------------------ */
 
@@ -280,7 +300,7 @@ int orc_compress_chunk_step(orc_t* s, const float* g, int64_t ld, int64_t k, flo
             z[j] = fadd(mw, ew[i]);
         }
         float sc = compress_chunk(z, k, (int32_t)C, n, words, err);
-        for (int64_t j = 0; j < n; ++j) ew[base + j] = err[j];
+        for (int64_t j = 0; j < n; ++j) ew[base + j] = store_err(s, err[j]);
         for (int64_t q = 0; q < nq; ++q) s->signs_w[(int64_t)w * NW + q0 + q] = words[q];
         s->scale_w[(int64_t)w * K + k] = sc;
         /* phase 2 (average), accumulated in worker order */
@@ -295,7 +315,7 @@ int orc_compress_chunk_step(orc_t* s, const float* g, int64_t ld, int64_t k, flo
         z[j] = fadd(avg, s->e_s[base + j]);
     }
     float ss = compress_chunk(z, k, (int32_t)C, n, words, err);
-    for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = err[j];
+    for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = store_err(s, err[j]);
     for (int64_t q = 0; q < nq; ++q) s->signs_s[q0 + q] = words[q];
     s->scale_s[k] = ss;
     /* phase 3 (scatter): every worker's momentum becomes the server result;

@@ -71,14 +71,14 @@ def close_vec_per_tensor(a, b, offsets, numels, tol):
 class Pair:
     """GPU optimizer and CPU oracle over the same workload."""
 
-    def __init__(self, wl, check_finite=0, variant=0):
+    def __init__(self, wl, check_finite=0, variant=0, error_storage=0):
         self.wl = wl
         self.x0 = workload.gen_params(wl)
         self.x = torch.from_numpy(self.x0.copy()).cuda()
-        hp = dict(wl.hp, check_finite=check_finite, variant=variant)
+        hp = dict(wl.hp, check_finite=check_finite, variant=variant, error_storage=error_storage)
         self.gpu = pkg.OneBitLamb(self.x, layers_of(wl), wl.W, wl.chunk, **hp)
         self.orc = oracle.Oracle(wl.offsets, wl.numels, wl.W, wl.chunk, wl.hp, self.x0,
-                                 variant=variant)
+                                 variant=variant, err_bf16=error_storage)
         self.ld = grad_ld(wl)
         self.t = 0
 
@@ -101,9 +101,11 @@ class Pair:
         s = self.gpu.state()
         N, W = self.wl.N, self.wl.W
         nw = -(-N // 32)
-        out = {k: s[k].cpu().numpy() for k in ("m", "v", "v_fresh", "e_s", "c_bar", "r_prev",
+        out = {k: s[k].cpu().numpy() for k in ("m", "v", "v_fresh", "c_bar", "r_prev",
                                                  "c_cur", "R_last", "Sx", "Su", "scale_s")}
-        out["e_w"] = s["e_w"].cpu().numpy()
+        # error buffers widened to binary32 (exact for bfloat16 storage)
+        out["e_s"] = s["e_s"].float().cpu().numpy()
+        out["e_w"] = s["e_w"].float().cpu().numpy()
         out["scale_w"] = s["scale_w"].cpu().numpy()
         out["signs_w"] = s["signs_w"].cpu().numpy().view(np.uint32)
         out["signs_s"] = s["signs_s"].cpu().numpy().view(np.uint32)

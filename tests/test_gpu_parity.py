@@ -17,8 +17,8 @@ def bert_mini(W=8, chunk=2048, grad="f32", **kw):
     return workload.custom("bert_mini", t, W=W, chunk=chunk, grad=grad, grad_std=1e-3, **kw)
 
 
-def run(wl, n_warm, n_comp, expect_bitwise=True, variant=0):
-    p = Pair(wl, variant=variant)
+def run(wl, n_warm, n_comp, expect_bitwise=True, variant=0, error_storage=0):
+    p = Pair(wl, variant=variant, error_storage=error_storage)
     diffs = 0
     for i in range(n_warm):
         p.warmup()
@@ -146,3 +146,25 @@ def test_nonfinite_gradients_propagate_like_the_oracle():
     np.testing.assert_array_equal(st["x"][fin], o.x[fin])
     assert np.isinf(o.R).any()
     np.testing.assert_array_equal(st["R_last"], o.R)
+
+
+# ---- bfloat16 error storage ---------------------------------------------------
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_bf16_error_storage(variant):
+    """Worker and server errors kept in bfloat16 (round to nearest even at
+    store): bit-exact against the oracle's bf16-storage variant, 20 steps on
+    the mini BERT table and the toy table, both method variants."""
+    run(bert_mini(W=8, chunk=2048), 10, 10, variant=variant, error_storage=1)
+    wl = workload.workloads()["tiny"]
+    run(wl, wl.warmup_steps, wl.compress_steps, variant=variant, error_storage=1)
+
+
+def test_bf16_error_storage_with_bf16_and_in_kernel_gradients():
+    t = workload.gpt2_tensors(2, 48, 192, 500, n_pos=64)
+    run(workload.custom("gpt2_mini", t, W=8, chunk=8192, grad="bf16", grad_std=1e-3), 2, 3,
+        error_storage=1)
+    t = workload.bert_tensors(1, 128, 512, 800)
+    wl = workload.custom("w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
+                         fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
+    run(wl, 1, 2, error_storage=1)

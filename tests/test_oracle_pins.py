@@ -446,3 +446,64 @@ def test_adam_variant_lossless_compression_is_frozen_variance_momentum_sgd():
     assert np.all(o.c_cur == 1.0)
     u = m_w / (np.sqrt(o.v.astype(np.float64)) + 1e-6) + 0.01 * x0
     np.testing.assert_allclose(o.x, x0 - 1e-3 * u, rtol=1e-6, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# bf16 error-storage variant
+# ---------------------------------------------------------------------------
+
+def test_bf16_storage_rounding_matches_torch():
+    """Round-to-nearest-even to bfloat16, checked against torch's conversion
+    (library routine) on random values, ties, signed zeros and infinities."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000)).astype(np.float32)
+    x[:6] = [0.0, -0.0, np.inf, -np.inf, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8]
+    ours = np.array([oracle.bf16_round(v) for v in x], dtype=np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(ours.view(np.uint32), ref.view(np.uint32))
+    assert np.isnan(oracle.bf16_round(float("nan")))
+
+
+def test_bf16_error_storage_rounds_the_fp32_error_once():
+    """From zero errors, one compression step of the bf16-storage variant
+    sends the same words and scales as the fp32 variant and keeps the
+    fp32 variant's new errors rounded to bfloat16."""
+    rng = np.random.default_rng(14)
+    states = []
+    for eb in (0, 1):
+        o = _fresh([3000, 700], 4, 512, HP, x0=(rng.standard_normal(3700) * 0 + 1).astype(np.float32))
+        o.err_bf16 = eb
+        o.m[:] = np.linspace(-1e-2, 1e-2, o.N, dtype=np.float32)
+        o.v[:] = 1e-4
+        o.freeze()
+        g = (np.sin(np.arange(4 * o.N, dtype=np.float64)).reshape(4, o.N) * 1e-2).astype(np.float32)
+        o.compress_step(g)
+        states.append(o)
+    a, b = states
+    np.testing.assert_array_equal(a.signs_w, b.signs_w)
+    np.testing.assert_array_equal(a.scale_w, b.scale_w)
+    want = np.array([oracle.bf16_round(v) for v in a.e_w.ravel()], np.float32).reshape(a.e_w.shape)
+    np.testing.assert_array_equal(b.e_w.view(np.uint32), want.view(np.uint32))
+
+
+def test_bf16_error_feedback_telescopes_within_storage_rounding():
+    """With bf16 error storage the error feedback still telescopes, up to one
+    bf16 rounding (2^-9 relative) of the kept error per step."""
+    rng = np.random.default_rng(15)
+    C = 1024
+    e = np.zeros(C, np.float32)
+    sent = np.zeros(C, np.float64)
+    fed = np.zeros(C, np.float64)
+    bound = np.zeros(C, np.float64)
+    for t in range(30):
+        p = (rng.standard_normal(C) * 1e-2).astype(np.float32)
+        z = (p + e).astype(np.float32)
+        bound += 0.5 * ulp32(z)
+        s, words, e_full = oracle.compress_chunk(z, 0, C)
+        e = np.array([oracle.bf16_round(v) for v in e_full], np.float32)
+        bits = np.unpackbits(words.view(np.uint8), bitorder="little")[:C]
+        sent += np.where(bits == 1, 1.0, -1.0) * float(s)
+        fed += p
+        bound += 0.5 * ulp32(e_full) + np.abs(e_full.astype(np.float64)) * 2.0 ** -8
+    assert np.all(np.abs(sent + e - fed) <= bound + 1e-12)
