@@ -524,7 +524,18 @@ def run_e2e(args, opt, wl, g, regen, t, ld):
         copy = torch.cuda.Stream()
         copied = [torch.cuda.Event(), torch.cuda.Event()]
         used = [torch.cuda.Event(), torch.cuda.Event()]
+        # per-step copy intervals, timed on the copy stream
+        c_beg = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps)]
+        c_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps)]
+        # one copy with nothing else running, for comparison
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        with torch.cuda.stream(copy):
+            a0.record(copy)
+            bufs[1].copy_(host, non_blocking=True)
+            a1.record(copy)
+        torch.cuda.synchronize()
+        alone_ms = a0.elapsed_time(a1)
         s0.record(compute)
         copy.wait_event(s0)
         for i in range(args.e2e_steps):
@@ -532,7 +543,9 @@ def run_e2e(args, opt, wl, g, regen, t, ld):
             with torch.cuda.stream(copy):
                 if i >= 2:
                     copy.wait_event(used[b])
+                c_beg[i].record(copy)
                 bufs[b].copy_(host, non_blocking=True)
+                c_end[i].record(copy)
                 copied[b].record(copy)
             compute.wait_event(copied[b])
             opt.compress_step(bufs[b])
@@ -541,13 +554,19 @@ def run_e2e(args, opt, wl, g, regen, t, ld):
             out_s.copy_(scales, non_blocking=True)
         s1.record(compute)
         torch.cuda.synchronize()
+        copy_ms = [a.elapsed_time(e) for a, e in zip(c_beg, c_end)]
         del bufs[1]
     sec = s0.elapsed_time(s1) / 1e3
-    return {"value": wl.N * args.e2e_steps / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": 1e3 * sec / args.e2e_steps,
-            "h2d_gbs": (h2d / (sec / args.e2e_steps) / 1e9) if h2d else None,
-            "overlap": "double-buffered gradients, copy stream || compute stream"}
+    out = {"value": wl.N * args.e2e_steps / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+           "ms_per_step": 1e3 * sec / args.e2e_steps,
+           "h2d_gbs": (h2d / (sec / args.e2e_steps) / 1e9) if h2d else None,
+           "overlap": "double-buffered gradients, copy stream || compute stream"}
+    if h2d:
+        out["copy_ms"] = [round(c, 3) for c in copy_ms]
+        out["copy_gbs_median"] = h2d / (statistics.median(copy_ms) / 1e3) / 1e9
+        out["copy_alone_gbs"] = h2d / (alone_ms / 1e3) / 1e9
+    return out
 
 
 def main():

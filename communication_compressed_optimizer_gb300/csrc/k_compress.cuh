@@ -89,16 +89,34 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity)
     return false;
 }
 
-// Word r of a warp's 128-element block: lanes 8r..8r+7 each hold a nibble of
-// 4 consecutive sign bits; OR-combine them across the 8 lanes.  Every lane of
-// the group returns the word.
-__device__ __forceinline__ uint32_t pack_nibbles(uint32_t nib, int lane)
+// Sign words of S slots at once (S a power of two, S <= 8).  In slot s the
+// word r of a warp's 128-element block is made of the nibbles nib[s] (4
+// consecutive sign bits) of lanes 8r..8r+7.  They are OR-combined across the
+// 8 lanes; while a lane still holds n > 1 slots it passes half of them to its
+// partner and keeps the other half.  Lane l returns word l/8 of slot
+// tree_block<S>(l) (lanes with l % 8 >= S hold duplicates).
+template <int S>
+__device__ __forceinline__ uint32_t pack_words(const uint32_t (&nib)[S], int lane)
 {
-    uint32_t v = nib << (4 * (lane & 7));
-    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    v |= __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    return v;
+    static_assert(S >= 1 && S <= 8 && (S & (S - 1)) == 0, "S a power of two");
+    uint32_t v[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) v[s] = nib[s] << (4 * (lane & 7));
+    int o = 1;
+#pragma unroll
+    for (int n = S; n > 1; n >>= 1, o <<= 1) {
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const uint32_t send = hi ? v[j] : v[j + n / 2];
+            const uint32_t keep = hi ? v[j + n / 2] : v[j];
+            v[j] = keep | __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+    }
+    uint32_t t = v[0];
+#pragma unroll
+    for (; o < 8; o <<= 1) t |= __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    return t;
 }
 
 template <int GK>
@@ -214,6 +232,27 @@ __device__ __forceinline__ float chunk_totals(const float* red, int lane)
 #pragma unroll
     for (int o = 1; o < LPC; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
+}
+
+// A worker's 4 gradients at tile offset off: from its ring slot a (binary32
+// or bfloat16 bits, widened exactly), or the values drawn in-kernel (gin).
+template <int GK>
+__device__ __forceinline__ void load_grad4(const unsigned char* a, int off, const float (&gin)[4],
+                                           float g[4])
+{
+    if constexpr (GK == kGradF32) {
+        const float4 v = *reinterpret_cast<const float4*>(a + off * 4);
+        g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+    } else if constexpr (GK == kGradBF16) {
+        const uint2 v = *reinterpret_cast<const uint2*>(a + off * 2);
+        g[0] = __uint_as_float(v.x << 16);
+        g[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        g[2] = __uint_as_float(v.y << 16);
+        g[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) g[c] = gin[c];
+    }
 }
 
 // Error-buffer element access: 4 consecutive values at element offset off,
@@ -350,6 +389,16 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                 }
             }
         }
+        // this thread's elements all draw from one kind of stream (true
+        // except at a boundary between a normal and a heavy-tailed tensor)
+        bool all_normal = true, all_heavy = true;
+        if constexpr (GK == kGradPhilox) {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                all_normal = all_normal && heavy[s] == 0u;
+                all_heavy = all_heavy && heavy[s] == 0xFu;
+            }
+        }
 
         // ---- item M: beta1 * m_old, kept for the whole tile ------------------
         float bm[SLOTS][4], acc[SLOTS][4];
@@ -374,65 +423,75 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             const void* eb = ring + (uint32_t)cp.plus(SL::kPerWorker - 1).slot * R::kSlot;
             cp = cp.plus(SL::kPerWorker);
             float z[SLOTS][4];
-            // in-kernel gradients: the normal draws of all slots first, as
-            // independent Philox chains (instruction-level parallelism), then
-            // the Student-t draws of the heavy-tailed tensors' elements
+            // in-kernel gradients.  Normal elements: the draws of all slots
+            // as independent Philox chains (instruction-level parallelism).
+            // Heavy-tailed elements: one Student-t draw each, again as
+            // independent chains when all of the thread's elements are heavy.
             float gin[SLOTS][4];
             if constexpr (GK == kGradPhilox) {
+                if (all_heavy) {
 #pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    gen::grads_normal4(G.seed, (uint64_t)(base + s * NT * 4 + tid * 4) >> 2, G.t,
-                                       (uint32_t)w, gin[s]);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) gin[s][c] = fmul(stdv[s][c], gin[s][c]);
-                }
-#pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    if (heavy[s]) {
+                    for (int s = 0; s < SLOTS; ++s)
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            if ((heavy[s] >> c) & 1u)
-                                gin[s][c] = fmul(G.heavy_scale,
-                                                 gen::student_t3(G.seed, base + s * NT * 4 + tid * 4 + c,
-                                                                 G.t, (uint32_t)w));
+                            gin[s][c] = fmul(G.heavy_scale,
+                                             gen::student_t3(G.seed, base + s * NT * 4 + tid * 4 + c,
+                                                             G.t, (uint32_t)w));
+                } else {
+#pragma unroll
+                    for (int s = 0; s < SLOTS; ++s) {
+                        gen::grads_normal4(G.seed, (uint64_t)(base + s * NT * 4 + tid * 4) >> 2, G.t,
+                                           (uint32_t)w, gin[s]);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) gin[s][c] = fmul(stdv[s][c], gin[s][c]);
+                    }
+                    if (!all_normal) {
+#pragma unroll
+                        for (int s = 0; s < SLOTS; ++s) {
+                            if (heavy[s]) {
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    if ((heavy[s] >> c) & 1u)
+                                        gin[s][c] = fmul(G.heavy_scale,
+                                                         gen::student_t3(G.seed, base + s * NT * 4 + tid * 4 + c,
+                                                                         G.t, (uint32_t)w));
+                            }
+                        }
                     }
                 }
             }
             // Per-element work, specialised at compile time for tiles whose
             // elements all exist (every tile but the last): no validity logic.
-            auto momentum_and_norms = [&](auto full_c) {
-                constexpr bool FULL = decltype(full_c)::value;
+            if (P.check_finite) {
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
                     const int off = s * NT * 4 + tid * 4;
                     float g[4];
-                    if constexpr (GK == kGradF32) {
-                        const float4 v = *reinterpret_cast<const float4*>(a + off * 4);
-                        g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
-                    } else if constexpr (GK == kGradBF16) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(a + off * 2);
-                        g[0] = __uint_as_float(v.x << 16);
-                        g[1] = __uint_as_float(v.x & 0xFFFF0000u);
-                        g[2] = __uint_as_float(v.y << 16);
-                        g[3] = __uint_as_float(v.y & 0xFFFF0000u);
-                    } else {
-                        // elements past N draw values too; they are masked below
+                    load_grad4<GK>(a, off, gin[s], g);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) g[c] = gin[s][c];
-                    }
-                    float ee[4];
+                    for (int c = 0; c < 4; ++c)
+                        if (c < nv[s] && !isfinite(g[c])) bad = true;
+                }
+            }
+            auto momentum_and_norms = [&](auto full_c) {
+                constexpr bool FULL = decltype(full_c)::value;
+                float part[SLOTS];
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    const int off = s * NT * 4 + tid * 4;
+                    float g[4], ee[4];
+                    load_grad4<GK>(a, off, gin[s], g);
                     load_err4<EB>(eb, off, ee);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const bool valid = FULL || c < nv[s];
-                        if (P.check_finite && valid && !isfinite(g[c])) bad = true;
                         const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
-                        z[s][c] = valid ? fadd(mw, ee[c]) : 0.0f;
+                        z[s][c] = (FULL || c < nv[s]) ? fadd(mw, ee[c]) : 0.0f;
                     }
-                    const float t = warp_tree128(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1]),
-                                                 fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3]));
-                    if (lane == 0) red[w & 1][s * NWARP + warp] = t;
+                    part[s] = fadd(fadd(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1])),
+                                   fadd(fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3])));
                 }
+                const float t = warp_trees128<SLOTS>(part, lane);
+                if (lane < SLOTS) red[w & 1][tree_block<SLOTS>(lane) * NWARP + warp] = t;
             };
             if (full_tile) momentum_and_norms(std::true_type{});
             else momentum_and_norms(std::false_type{});
@@ -441,30 +500,31 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             if (tid == 0) issue_ready();
             const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
             const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
-            // this thread's sign word (lanes 0, 8, 16, 24) and error elements
-            uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld + (base + warp * 128) / 32 + (lane >> 3);
+            // this thread's error elements, and the sign words its lane stores
             const int64_t eoff = (int64_t)w * P.Np + base + tid * 4;
+            uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld + (base + warp * 128) / 32 + (lane >> 3);
             auto signs_and_errors = [&](auto full_c) {
                 constexpr bool FULL = decltype(full_c)::value;
+                uint32_t nib[SLOTS];
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
                     const float sc = (CPT == 1) ? sq : __shfl_sync(0xFFFFFFFFu, sq, qsrc[s]);
                     const float nsc = -sc;
-                    uint32_t nib = 0u;
                     float en[4];
+                    nib[s] = 0u;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const bool valid = FULL || c < nv[s];
                         const bool neg = z[s][c] < 0.0f;       // +0, -0 and NaN send +1
                         const float ss = neg ? nsc : sc;
-                        if (!neg && valid) nib |= 1u << c;
+                        if (!neg && valid) nib[s] |= 1u << c;
                         en[c] = valid ? fsub(z[s][c], ss) : 0.0f;
                         acc[s][c] = fadd(acc[s][c], ss);
                     }
-                    const uint32_t word = pack_nibbles(nib, lane);
-                    if ((lane & 7) == 0) sw[s * NT * 4 / 32] = word;
                     store_err4<EB>(D.e_w, eoff + s * NT * 4, en);
                 }
+                const uint32_t word = pack_words<SLOTS>(nib, lane);
+                if ((lane & 7) < SLOTS) sw[tree_block<SLOTS>(lane) * (NT * 4 / 32)] = word;
             };
             if (full_tile) signs_and_errors(std::true_type{});
             else signs_and_errors(std::false_type{});
@@ -480,84 +540,105 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             const float* vf_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(2).slot * R::kSlot);
             cp = cp.plus(nsrv);
             float y[SLOTS][4], vz[SLOTS][4], vfo[SLOTS][4];
-            const float Wf = (float)W;
+            auto average_and_norms = [&](auto full_c) {
+                constexpr bool FULL = decltype(full_c)::value;
+                float part[SLOTS];
 #pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                float ee[4];
-                load_err4<EB>(es_in, off, ee);
-                if constexpr (!ADAM) {
-                    const float4 v = *reinterpret_cast<const float4*>(v_in + off);
-                    const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
-                    vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
-                    vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
-                }
+                for (int s = 0; s < SLOTS; ++s) {
+                    const int off = s * NT * 4 + tid * 4;
+                    float ee[4];
+                    load_err4<EB>(es_in, off, ee);
+                    if constexpr (!ADAM) {
+                        const float4 v = *reinterpret_cast<const float4*>(v_in + off);
+                        const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
+                        vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
+                        vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
+                    }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_tile || c < nv[s];
-                    y[s][c] = valid ? fadd(fdiv(acc[s][c], Wf), ee[c]) : 0.0f;
+                    for (int c = 0; c < 4; ++c)
+                        y[s][c] = (FULL || c < nv[s]) ? fadd(div_w(acc[s][c], P), ee[c]) : 0.0f;
+                    part[s] = fadd(fadd(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1])),
+                                   fadd(fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3])));
                 }
-                const float t = warp_tree128(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1]),
-                                             fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3]));
-                if (lane == 0) red[W & 1][s * NWARP + warp] = t;
-            }
+                const float t = warp_trees128<SLOTS>(part, lane);
+                if (lane < SLOTS) red[W & 1][tree_block<SLOTS>(lane) * NWARP + warp] = t;
+            };
+            if (full_tile) average_and_norms(std::true_type{});
+            else average_and_norms(std::false_type{});
             if (__syncthreads_or(lost)) goto abort;
             released += nsrv;
             if (tid == 0) issue_ready();
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
             const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
 
+            // Per-tensor max of rho: a running max per thread, flushed into the
+            // tile's shared per-tensor slots (or global, past kMaxChunkLayers)
+            // whenever the tensor changes.  A full tile inside one tensor needs
+            // no per-element tensor tracking.
             int l = l0;
             int64_t lend = D.layer_end[l];
+            const bool one_tensor = full_tile && lend >= base + TILE;
             int lcur = -1;
             uint32_t runmax = 0u;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int off = s * NT * 4 + tid * 4;
-                const float ss = (CPT == 1) ? ssq : __shfl_sync(0xFFFFFFFFu, ssq, qsrc[s]);
-                uint32_t nib = 0u;
-                float es[4], mn[4], vf[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const bool valid = full_tile || c < nv[s];
-                    const bool pos = !(y[s][c] < 0.0f);
-                    const float sgn = pos ? ss : -ss;
-                    nib |= (valid && pos) ? (1u << c) : 0u;
-                    es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
-                    mn[c] = valid ? sgn : 0.0f;
-                    if constexpr (ADAM) continue;
-                    // reconstructed gradient and fresh second moment
-                    const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
-                    vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
-                    if (valid) {
-                        float rho = fdiv(fadd(fsqrt(vz[s][c]), P.eps), fadd(fsqrt(vf[c]), P.eps));
-                        if (rho != rho) rho = __int_as_float(0x7F800000);
-                        const int64_t i = base + off + c;
-                        while (i >= lend) { ++l; lend = D.layer_end[l]; }
-                        if (l != lcur) {
-                            if (lcur >= 0) {
-                                if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
-                                else atomicMax(&D.Rmax[lcur], runmax);
-                            }
-                            lcur = l;
-                            runmax = 0u;
-                        }
-                        runmax = max(runmax, __float_as_uint(rho));
-                    }
+            auto flush_max = [&]() {
+                if (lcur >= 0) {
+                    if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
+                    else atomicMax(&D.Rmax[lcur], runmax);
                 }
-                const uint32_t word = pack_nibbles(nib, lane);
-                if ((lane & 7) == 0)
-                    D.signs_s[(base + s * NT * 4 + warp * 128) / 32 + (lane >> 3)] = word;
-                store_err4<EB>(D.e_s, base + off, es);
-                *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-                if constexpr (!ADAM)
-                    *reinterpret_cast<float4*>(D.v_fresh + base + off) =
-                        make_float4(vf[0], vf[1], vf[2], vf[3]);
-            }
-            if (lcur >= 0) {
-                if (lcur - l0 < kMaxChunkLayers) atomicMax(&lmax[lcur - l0], runmax);
-                else atomicMax(&D.Rmax[lcur], runmax);
-            }
+            };
+            auto recompress_and_scatter = [&](auto full_c, auto one_c) {
+                constexpr bool FULL = decltype(full_c)::value;
+                constexpr bool ONE = decltype(one_c)::value;
+                if constexpr (ONE && !ADAM) lcur = l0;
+                uint32_t nib[SLOTS];
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    const int off = s * NT * 4 + tid * 4;
+                    const float ss = (CPT == 1) ? ssq : __shfl_sync(0xFFFFFFFFu, ssq, qsrc[s]);
+                    const float nss = -ss;
+                    float es[4], mn[4], vf[4];
+                    nib[s] = 0u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const bool valid = FULL || c < nv[s];
+                        const bool neg = y[s][c] < 0.0f;
+                        const float sgn = neg ? nss : ss;
+                        if (!neg && valid) nib[s] |= 1u << c;
+                        es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
+                        mn[c] = valid ? sgn : 0.0f;
+                        if constexpr (ADAM) continue;
+                        // reconstructed gradient and fresh second moment
+                        const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
+                        vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
+                        if (valid) {
+                            float rho = fdiv(fadd(fsqrt(vz[s][c]), P.eps), fadd(fsqrt(vf[c]), P.eps));
+                            if (rho != rho) rho = __int_as_float(0x7F800000);
+                            if constexpr (!ONE) {
+                                const int64_t i = base + off + c;
+                                while (i >= lend) { ++l; lend = D.layer_end[l]; }
+                                if (l != lcur) {
+                                    flush_max();
+                                    lcur = l;
+                                    runmax = 0u;
+                                }
+                            }
+                            runmax = max(runmax, __float_as_uint(rho));
+                        }
+                    }
+                    store_err4<EB>(D.e_s, base + off, es);
+                    *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
+                    if constexpr (!ADAM)
+                        *reinterpret_cast<float4*>(D.v_fresh + base + off) =
+                            make_float4(vf[0], vf[1], vf[2], vf[3]);
+                }
+                const uint32_t word = pack_words<SLOTS>(nib, lane);
+                if ((lane & 7) < SLOTS)
+                    D.signs_s[(base + warp * 128) / 32 + (lane >> 3) + tree_block<SLOTS>(lane) * (NT * 4 / 32)] = word;
+            };
+            if (one_tensor) recompress_and_scatter(std::true_type{}, std::true_type{});
+            else if (full_tile) recompress_and_scatter(std::true_type{}, std::false_type{});
+            else recompress_and_scatter(std::false_type{}, std::false_type{});
+            flush_max();
             if (warp == 0 && lane_stores_scale) D.scale_s[kq] = ssq;
         }
         __syncthreads();

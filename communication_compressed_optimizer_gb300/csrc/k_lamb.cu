@@ -16,7 +16,23 @@ constexpr int kBlock = kNT * 4 * kSlots;   // 4096 elements per CTA
 
 __device__ __forceinline__ int first_layer_of_block(const Problem& P, const Dev& D, int64_t b0)
 {
-    return D.chunk_l0[b0 / P.C];   // the chunk holding b0 starts at or before it
+    return D.chunk_l0[b0 >> P.log2c];   // the chunk holding b0 starts at or before it
+}
+
+// Momentum of 4 elements at idx (a multiple of 4): the dense copy, or (msig)
+// the server's sign bits of this step times its chunk scale.
+__device__ __forceinline__ void update_momentum4(const Problem& P, const Dev& D, int msig, int64_t idx,
+                                                 float mm[4])
+{
+    if (msig) {
+        const uint32_t word = D.signs_s[idx >> 5];
+        const float sc = D.scale_s[idx >> P.log2c];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mm[c] = ((word >> ((idx & 31) + c)) & 1u) ? sc : -sc;
+    } else {
+        const float4 m4 = *reinterpret_cast<const float4*>(D.m + idx);
+        mm[0] = m4.x; mm[1] = m4.y; mm[2] = m4.z; mm[3] = m4.w;
+    }
 }
 
 // ---- update: x = x - (lr c_l) (m / (sqrt(v) + eps) + wd x) ----------------
@@ -32,20 +48,38 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
     int l = first_layer_of_block(P, D, b0);
     int64_t lend = D.layer_end[l];
     float gcl = D.gc[l];
+    if (b0 + kBlock <= P.N && lend >= b0 + kBlock) {
+        // the whole block lies in tensor l: every load is issued before any
+        // arithmetic or store
+        float mm[kSlots][4], vv[kSlots][4], xv[kSlots][4];
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            const int64_t idx = b0 + s * kNT * 4 + tid * 4;
+            update_momentum4(P, D, msig, idx, mm[s]);
+            const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
+            const float4 x4 = *reinterpret_cast<const float4*>(x + idx);
+            vv[s][0] = v4.x; vv[s][1] = v4.y; vv[s][2] = v4.z; vv[s][3] = v4.w;
+            xv[s][0] = x4.x; xv[s][1] = x4.y; xv[s][2] = x4.z; xv[s][3] = x4.w;
+        }
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float d = fadd(fsqrt(vv[s][c]), P.eps);
+                const float u = fadd(fdiv(mm[s][c], d), fmul(P.wd, xv[s][c]));
+                xv[s][c] = fsub(xv[s][c], fmul(gcl, u));
+            }
+            *reinterpret_cast<float4*>(x + b0 + s * kNT * 4 + tid * 4) =
+                make_float4(xv[s][0], xv[s][1], xv[s][2], xv[s][3]);
+        }
+        return;
+    }
 #pragma unroll
     for (int s = 0; s < kSlots; ++s) {
         const int64_t idx = b0 + s * kNT * 4 + tid * 4;
         if (idx >= P.N) break;
         float mm[4];
-        if (msig) {
-            const uint32_t word = D.signs_s[idx / 32];
-            const float sc = D.scale_s[idx / P.C];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) mm[c] = ((word >> ((idx & 31) + c)) & 1u) ? sc : -sc;
-        } else {
-            const float4 m4 = *reinterpret_cast<const float4*>(D.m + idx);
-            mm[0] = m4.x; mm[1] = m4.y; mm[2] = m4.z; mm[3] = m4.w;
-        }
+        update_momentum4(P, D, msig, idx, mm);
         const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
         const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
         const bool full = idx + 4 <= P.N;
@@ -126,7 +160,6 @@ __global__ void __launch_bounds__(kNT) k_warmup_moments(const Problem P, const D
     const int64_t b0 = (int64_t)blockIdx.x * kBlock;
     int l = first_layer_of_block(P, D, b0);
     int64_t lend = D.layer_end[l];
-    const float Wf = (float)P.W;
     bool bad = false;
 #pragma unroll 1
     for (int s = 0; s < kSlots; ++s) {
@@ -175,7 +208,7 @@ __global__ void __launch_bounds__(kNT) k_warmup_moments(const Problem P, const D
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 if (c < nv) {
-                    const float gb = fdiv(acc[c], Wf);
+                    const float gb = div_w(acc[c], P);
                     mm[c] = fadd(fmul(P.beta1, mm[c]), fmul(P.omega1, gb));
                     vv[c] = fadd(fmul(P.beta2, vv[c]), fmul(P.omega2, fmul(gb, gb)));
                     const float d = fadd(fsqrt(vv[c]), P.eps);

@@ -230,6 +230,10 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     P.check_finite = hp->check_finite;
     P.adam = hp->variant == 1 ? 1 : 0;
     P.ebf16 = hp->error_storage == 1 ? 1 : 0;
+    P.log2c = 0;
+    while ((1 << P.log2c) < p.C) ++P.log2c;
+    P.w_pow2 = (p.W & (p.W - 1)) == 0 ? 1 : 0;
+    P.inv_w = 1.0f / (float)p.W;
 
     char* ws = static_cast<char*>(workspace_dev);
     Dev& D = c->D;

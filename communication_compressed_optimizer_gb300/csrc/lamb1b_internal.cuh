@@ -26,6 +26,9 @@ struct Problem {
     int32_t check_finite;
     int32_t adam;       // 1-bit Adam variant: no layerwise coefficient, no fresh variance
     int32_t ebf16;      // e_w and e_s stored as bfloat16
+    int32_t log2c;      // C = 2^log2c
+    int32_t w_pow2;     // W is a power of two
+    float inv_w;        // 1 / W (exact when w_pow2)
 };
 
 // Device pointers into the caller's workspace.
@@ -92,6 +95,52 @@ __device__ __forceinline__ float warp_tree128(float f0, float f1, float f2, floa
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
+}
+
+// fl(a / W).  For W = 2^k the quotient a 2^-k is the exact product with the
+// exact reciprocal, so one rounded multiplication gives the same bits as the
+// rounded division for every a (zeros, subnormals, infinities, NaN).
+__device__ __forceinline__ float div_w(float a, const Problem& P)
+{
+    return P.w_pow2 ? fmul(a, P.inv_w) : fdiv(a, (float)P.W);
+}
+
+// Pairwise trees of S independent 128-leaf blocks at once (S a power of two,
+// S <= 32).  Lane l holds leaf-group sums v[s] = ((f0+f1)+(f2+f3)) of leaves
+// 4l..4l+3 of block s.  The butterfly over partners 1, 2, 4, 8, 16 is the same
+// tree as warp_tree128 for every block, but while a lane still holds n > 1
+// blocks it passes half of them to its partner and keeps the other half, so S
+// blocks cost about as many exchanges as two.  Lane l returns the total of
+// block tree_block<S>(l).
+template <int S>
+__device__ __forceinline__ int tree_block(int lane)
+{
+    int b = 0, o = 1;
+#pragma unroll
+    for (int n = S; n > 1; n >>= 1, o <<= 1)
+        if (lane & o) b += n / 2;
+    return b;
+}
+
+template <int S>
+__device__ __forceinline__ float warp_trees128(float (&v)[S], int lane)
+{
+    static_assert(S >= 1 && S <= 32 && (S & (S - 1)) == 0, "S a power of two");
+    int o = 1;
+#pragma unroll
+    for (int n = S; n > 1; n >>= 1, o <<= 1) {
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const float send = hi ? v[j] : v[j + n / 2];
+            const float keep = hi ? v[j + n / 2] : v[j];
+            v[j] = fadd(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (; o < 32; o <<= 1) t = fadd(t, __shfl_xor_sync(0xFFFFFFFFu, t, o));
+    return t;
 }
 
 // binary32 -> bfloat16 bits, round to nearest even; NaN -> 0x7FC0
