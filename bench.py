@@ -47,6 +47,10 @@ def parse_args():
                    help="1-bit LAMB (default) or the 1-bit Adam variant")
     p.add_argument("--errors", choices=("f32", "bf16"), default="f32",
                    help="storage of the worker and server error buffers")
+    p.add_argument("--chunk", type=int, default=0,
+                   help="override the workload's chunk size C (the named workloads fix it)")
+    p.add_argument("--workers", type=int, default=0,
+                   help="override the workload's worker count W (the named workloads fix it)")
     p.add_argument("--max-params", type=int, default=0,
                    help="keep only the leading tensors up to this many parameters (profiling)")
     p.add_argument("--warmup-stage-steps", type=int, default=-1,
@@ -60,6 +64,12 @@ def parse_args():
 
 def get_workload(args):
     wl = workload.workloads()[args.workload]
+    if args.chunk:
+        wl.chunk = args.chunk
+        wl.name = f"{wl.name}[C={args.chunk}]"
+    if args.workers:
+        wl.W = args.workers
+        wl.name = f"{wl.name}[W={args.workers}]"
     if args.max_params:
         keep, n = [], 0
         for name, shape in wl.tensors:
