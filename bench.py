@@ -340,6 +340,30 @@ def run_reference(args, world, rank):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def live_copy_gbs(gib=2, reps=5):
+    """Bandwidth of a plain device-to-device copy on this GPU, measured now
+    (bytes read + bytes written per second, best of reps, 2 GiB each way).
+    Context for the roofline fraction: the peak the fraction divides by was
+    measured once for the pool, and GB300s differ by a few percent."""
+    import torch
+    n = (gib << 30) // 4
+    src = torch.empty(n, dtype=torch.float32, device="cuda").fill_(1.0)
+    dst = torch.empty_like(src)
+    st = torch.cuda.current_stream()
+    best = float("inf")
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(st)
+        dst.copy_(src)
+        b.record(st)
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) / 1e3)
+    del src, dst
+    torch.cuda.empty_cache()
+    return 2 * n * 4 / best / 1e9
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -422,10 +446,12 @@ def run_ours(args, world, rank, local):
     k_avg = statistics.mean(kern_ms)
     achieved = kb / (k_avg / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
+    copy_now = live_copy_gbs()
     roofline = {"bound": "hbm", "kernel": "k_compress (fused worker+server pass)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": traffic, "alg_bytes_per_launch": kb, "kernel_ms": k_avg}
+                "traffic": traffic, "alg_bytes_per_launch": kb, "kernel_ms": k_avg,
+                "live_copy_gbs": copy_now, "frac_of_live_copy": achieved / copy_now}
     if wl.grad == "philox":
         # gradients drawn in the kernel: bound by instruction issue, not HBM
         inst = profiled_instructions(wl.name)
@@ -437,7 +463,8 @@ def run_ours(args, world, rank, local):
                         "peak_source": "152 SMs x 4 schedulers x 32 lanes x 2070 MHz",
                         "traffic": None, "thread_inst_per_launch": inst, "kernel_ms": k_avg,
                         "hbm": {"achieved": achieved, "peak": peak, "unit": "GB/s",
-                                "frac": achieved / peak, "alg_bytes_per_launch": kb}}
+                                "frac": achieved / peak, "alg_bytes_per_launch": kb,
+                                "live_copy_gbs": copy_now}}
 
     # per-tensor coefficients after the timed steps: where the soft thresholds
     # and clip bounds are active

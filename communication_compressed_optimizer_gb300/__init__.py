@@ -161,6 +161,14 @@ class OneBitLamb:
         _abi.check("lamb1b_set_counters",
                    self._lib.lamb1b_set_counters(self._ctx, int(t), int(n_warmup), int(stage)))
 
+    def set_fault_injection(self, skip_copy=-1, wait_tries=0):
+        """Testing hook: the first CTA of later compression steps leaves out
+        bulk copy number skip_copy (-1: none); every copy wait gives up after
+        wait_tries try_wait calls (0: the default).  A step that gave up is
+        reported by check_status() as a timeout."""
+        _abi.check("lamb1b_set_fault_injection",
+                   self._lib.lamb1b_set_fault_injection(self._ctx, int(skip_copy), int(wait_tries)))
+
     def set_trace_events(self, events):
         """events: 4 torch.cuda.Event objects (or None to stop tracing).
         Each later step records them before its first kernel and after each

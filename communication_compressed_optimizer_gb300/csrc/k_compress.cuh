@@ -79,12 +79,11 @@ __device__ __forceinline__ bool try_wait(uint64_t* bar, uint32_t parity)
 }  // namespace tma
 
 // Bounded wait for a stage: try_wait suspends for a hardware-defined time per
-// call, so this gives up after seconds, never hangs.
-constexpr uint32_t kMaxWaitTries = 1u << 24;
-
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity)
+// call, so with the default limit (P.wait_tries = 2^24) this gives up after
+// seconds, never hangs.
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint32_t tries)
 {
-    for (uint32_t it = 0; it < kMaxWaitTries; ++it)
+    for (uint32_t it = 0; it < tries; ++it)
         if (tma::try_wait(bar, parity)) return true;
     return false;
 }
@@ -156,11 +155,13 @@ struct RingPos {
 };
 
 // Producer side: issue the bulk copies of item r of tile t whose first slot
-// position is p; called by thread 0 only.
+// position is p (number pos in this CTA's sequence); called by thread 0 only.
+// The fault-injection hook leaves out the copy at position P.skip_copy of the
+// first CTA, so that the wait for it can only run out.
 template <int TILE, int SG, int NSLOT, bool ADAM, bool EB>
-__device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, const Problem& P,
-                                           const Dev& D, const Grads& G, unsigned char* ring,
-                                           uint64_t* full)
+__device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, int pos,
+                                           const Problem& P, const Dev& D, const Grads& G,
+                                           unsigned char* ring, uint64_t* full)
 {
     using R = Ring<TILE>;
     const int W = P.W;
@@ -170,6 +171,7 @@ __device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, c
     const unsigned char* es = reinterpret_cast<const unsigned char*>(D.e_s);
     const int64_t esz = EB ? 2 : 4;
     auto copy = [&](int k, const void* src, uint32_t bytes) {
+        if (pos + k == P.skip_copy && blockIdx.x == 0) return;
         const int sl = p.plus(k).slot;
         tma::arrive_expect_tx(&full[sl], bytes);
         tma::load(ring + (uint32_t)sl * R::kSlot, src, bytes, &full[sl]);
@@ -196,12 +198,12 @@ __device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, c
 
 // Consumer side: wait for n consecutive slots starting at p.
 template <int NSLOT>
-__device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int n)
+__device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int n, uint32_t tries)
 {
     bool ok = true;
     for (int k = 0; k < n; ++k) {
         const RingPos<NSLOT> q = p.plus(k);
-        ok &= wait_stage(&full[q.slot], q.phase);
+        ok &= wait_stage(&full[q.slot], q.phase, tries);
     }
     return ok;
 }
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             const int n = SL::slots(issue_r, W);
             if (issue_pos + n > released + NSLOT) break;
             issue_item<TILE, SG, NSLOT, ADAM, EB>(blockIdx.x + issue_tile * gridDim.x, issue_r, ip,
-                                              P, D, G, ring, full);
+                                                  issue_pos, P, D, G, ring, full);
             issue_pos += n;
             ip = ip.plus(n);
             if (++issue_r == TPC) { issue_r = 0; ++issue_tile; }
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
         // ---- item M: beta1 * m_old, kept for the whole tile ------------------
         float bm[SLOTS][4], acc[SLOTS][4];
         {
-            if (!wait_slots<NSLOT>(full, cp, 1)) lost = true;
+            if (!wait_slots<NSLOT>(full, cp, 1, P.wait_tries)) lost = true;
             const float* a = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
             cp = cp.plus(1);
 #pragma unroll
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
 
         // ---- phase 1: every worker compresses its chunks ----------------------
         for (int w = 0; w < W; ++w) {
-            if (!wait_slots<NSLOT>(full, cp, SL::kPerWorker)) lost = true;
+            if (!wait_slots<NSLOT>(full, cp, SL::kPerWorker, P.wait_tries)) lost = true;
             const unsigned char* a = ring + (uint32_t)cp.slot * R::kSlot;
             const void* eb = ring + (uint32_t)cp.plus(SL::kPerWorker - 1).slot * R::kSlot;
             cp = cp.plus(SL::kPerWorker);
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
         // ---- phases 2 and 3: server average, recompression, scatter ----------
         {
             const int nsrv = SL::kServer + (ADAM ? 0 : 1);      // S (and F) slots
-            if (!wait_slots<NSLOT>(full, cp, nsrv)) lost = true;
+            if (!wait_slots<NSLOT>(full, cp, nsrv, P.wait_tries)) lost = true;
             const float* es_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
             const float* v_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(1).slot * R::kSlot);
             const float* vf_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(2).slot * R::kSlot);
@@ -665,7 +667,7 @@ abort:
         for (int k = issue_pos - released; k > 0; --k) {
             q.slot -= 1;
             if (q.slot < 0) { q.slot += NSLOT; q.phase ^= 1u; }
-            wait_stage(&full[q.slot], q.phase);
+            wait_stage(&full[q.slot], q.phase, P.wait_tries);
         }
     }
     __syncthreads();

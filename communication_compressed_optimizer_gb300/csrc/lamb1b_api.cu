@@ -230,6 +230,8 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     P.check_finite = hp->check_finite;
     P.adam = hp->variant == 1 ? 1 : 0;
     P.ebf16 = hp->error_storage == 1 ? 1 : 0;
+    P.wait_tries = lamb1b::kDefaultWaitTries;
+    P.skip_copy = -1;
     P.log2c = 0;
     while ((1 << P.log2c) < p.C) ++P.log2c;
     P.w_pow2 = (p.W & (p.W - 1)) == 0 ? 1 : 0;
@@ -416,6 +418,14 @@ extern "C" int lamb1b_set_trace_events(lamb1b_ctx* ctx, void* const* events, int
     }
     for (int i = 0; i < 4; ++i) ctx->ev[i] = static_cast<cudaEvent_t>(events[i]);
     ctx->tracing = true;
+    return LAMB1B_OK;
+}
+
+extern "C" int lamb1b_set_fault_injection(lamb1b_ctx* ctx, int32_t skip_copy, uint32_t wait_tries)
+{
+    if (!ctx || skip_copy < -1) return LAMB1B_ERR_ARG;
+    ctx->P.skip_copy = skip_copy;
+    ctx->P.wait_tries = wait_tries ? wait_tries : lamb1b::kDefaultWaitTries;
     return LAMB1B_OK;
 }
 

@@ -13,6 +13,10 @@ namespace lamb1b {
 constexpr int kGranule = 256;        // level-0 block of the canonical pairwise tree
 constexpr int kMaxChunkLayers = 64;  // per-chunk layer slots kept in shared memory
 
+// Default bound of a shared-memory copy wait, in mbarrier.try_wait calls
+// (each suspends for a hardware-defined time): seconds, far beyond any copy.
+constexpr uint32_t kDefaultWaitTries = 1u << 24;
+
 struct Problem {
     int64_t N;        // parameters
     int64_t Np;       // padded vector length: a multiple of max(C, 4096) >= K * C
@@ -29,6 +33,8 @@ struct Problem {
     int32_t log2c;      // C = 2^log2c
     int32_t w_pow2;     // W is a power of two
     float inv_w;        // 1 / W (exact when w_pow2)
+    uint32_t wait_tries; // bound of every shared-memory copy wait (try_wait calls)
+    int32_t skip_copy;   // fault injection: copy position left out by CTA 0, or -1
 };
 
 // Device pointers into the caller's workspace.

@@ -234,6 +234,20 @@ int lamb1b_check_status(lamb1b_ctx* ctx, void* stream);
  * Errors: ARG for other n or NULL events with n == 4. */
 int lamb1b_set_trace_events(lamb1b_ctx* ctx, void* const* events, int32_t n);
 
+/* Testing hook for the failure path of the compression step (the paper has
+ * no counterpart).  The compression kernel stages its inputs through shared
+ * memory with bulk copies and waits for each with a bounded mbarrier wait.
+ * skip_copy >= 0 makes the first CTA of every later compression step leave
+ * out the copy at that position of its copy sequence (0 = the first tile's
+ * momentum, then per worker its gradient and error, ...), so the wait for it
+ * can only run out; skip_copy = -1 turns this off.  wait_tries bounds every
+ * wait, in mbarrier.try_wait calls; 0 restores the default (2^24, seconds).
+ * A step whose wait ran out stops early, records LAMB1B_ERR_TIMEOUT for
+ * lamb1b_check_status and leaves the optimizer state undefined (restore it
+ * from a checkpoint); the CUDA context stays usable.  No GPU fault is raised.
+ * Errors: ARG for a NULL ctx or skip_copy < -1. */
+int lamb1b_set_fault_injection(lamb1b_ctx* ctx, int32_t skip_copy, uint32_t wait_tries);
+
 /* Allocation-free per-tensor sums of squares (the paper has no counterpart;
  * this is a convenience for callers that cannot allocate device memory).
  *

@@ -109,6 +109,85 @@ def test_checkpoint_resume_is_bitwise():
         assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
 
 
+def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers():
+    """Failure path without a GPU fault: the first CTA leaves out one of its
+    shared-memory bulk copies, so its bounded wait for it runs out.  The step
+    reports LAMB1B_ERR_TIMEOUT, the context stays usable, and restoring the
+    state saved before the step continues bit for bit like an uninterrupted
+    run.  Skipped copies: the first tile's momentum, a worker's gradient, a
+    worker's error, the server error, the fresh second moment."""
+    wl = _bert_mini()
+    ld = grad_ld(wl)
+    ref, xr = _run_gpu_only(wl, 3, 4)
+    a, xa = _run_gpu_only(wl, 3, 2)
+    sa = a.state()
+    saved = {k: v.clone() for k, v in sa.items() if isinstance(v, torch.Tensor)}
+    counters = (sa["t"], sa["n_warmup"], sa["stage"])
+    x_saved = xa.clone()
+    t = counters[0]
+    # copy positions of the first tile: 0 momentum, 1 + 2w gradient of worker
+    # w, 2 + 2w its error, 1 + 2W server error, 2 + 2W frozen v, 3 + 2W v_fresh
+    W = wl.W
+    for skip in (0, 5, 2 * W, 1 + 2 * W, 3 + 2 * W):
+        a.set_fault_injection(skip, 2000)
+        a.compress_step(device_grads(wl, t, ld))
+        with pytest.raises(pkg.Lamb1bError) as e:
+            a.check_status()
+        assert e.value.code == _abi.ERR_TIMEOUT, skip
+        a.check_status()                      # cleared
+        cur = a.state()
+        for k, v in saved.items():
+            cur[k].copy_(v)
+        xa.copy_(x_saved)
+        a.set_counters(*counters)
+    a.set_fault_injection(-1, 0)
+    for _ in range(2):
+        a.compress_step(device_grads(wl, t, ld))
+        t += 1
+    a.check_status()
+    torch.cuda.synchronize()
+    assert torch.equal(xa.view(torch.int32), xr.view(torch.int32))
+    sr, sb = ref.state(), a.state()
+    for k in ("m", "v", "v_fresh", "e_s", "e_w", "signs_w", "signs_s", "scale_w", "scale_s",
+              "r_prev", "c_cur", "c_bar"):
+        assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
+
+
+def test_compress_step_replays_from_a_cuda_graph():
+    """A compression step only enqueues kernels on the caller's stream (no
+    host synchronisation, no allocation), so it can be captured once in a
+    CUDA graph and replayed: three replays of a captured step give the same
+    device state, bit for bit, as three direct calls with the same gradients.
+    (The host step counter advances on direct calls only.)"""
+    wl = _bert_mini()
+    ld = grad_ld(wl)
+    a, xa = _run_gpu_only(wl, 3, 1)
+    b, xb = _run_gpu_only(wl, 3, 1)
+    g = device_grads(wl, 50, ld)
+    for _ in range(3):
+        a.compress_step(g)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        b.compress_step(g)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(xa.view(torch.int32), xb.view(torch.int32))
+    sa, sb = a.state(), b.state()
+    for k in ("m", "v", "v_fresh", "e_s", "e_w", "signs_w", "signs_s", "scale_w", "scale_s",
+              "r_prev", "c_cur", "c_bar", "R_last"):
+        assert torch.equal(sa[k].view(torch.int32), sb[k].view(torch.int32)), k
+
+
+def test_fault_injection_arguments():
+    wl = _bert_mini()
+    x = torch.from_numpy(workload.gen_params(wl)).cuda()
+    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    with pytest.raises(pkg.Lamb1bError):
+        opt.set_fault_injection(-2, 0)
+    opt.set_fault_injection(-1, 0)
+
+
 def test_nonfinite_gradients_are_flagged():
     wl = _bert_mini()
     x = torch.from_numpy(workload.gen_params(wl)).cuda()
