@@ -278,8 +278,7 @@ template <bool EB>
 __device__ __forceinline__ void store_err4(void* base, int64_t off, const float e[4])
 {
     if constexpr (EB) {
-        const uint2 v = make_uint2(bf16_bits(e[0]) | (bf16_bits(e[1]) << 16),
-                                   bf16_bits(e[2]) | (bf16_bits(e[3]) << 16));
+        const uint2 v = make_uint2(bf16x2_bits(e[0], e[1]), bf16x2_bits(e[2], e[3]));
         *reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + off) = v;
     } else {
         *reinterpret_cast<float4*>(static_cast<float*>(base) + off) = make_float4(e[0], e[1], e[2], e[3]);

@@ -4,6 +4,7 @@
 // warp-level pairwise tree, sign-word packing, layer lookup).
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "philox.cuh"
@@ -149,11 +150,16 @@ __device__ __forceinline__ float warp_trees128(float (&v)[S], int lane)
     return t;
 }
 
-// binary32 -> bfloat16 bits, round to nearest even; NaN -> 0x7FC0
-__device__ __forceinline__ uint32_t bf16_bits(float x)
+// Two binary32 values -> packed bfloat16 bits (lo in bits 0-15), each
+// rounded to nearest even by one hardware conversion (cvt.rn.bf16x2.f32);
+// a NaN is stored as 0x7FC0.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi)
 {
-    const uint32_t b = __float_as_uint(x);
-    return (x != x) ? 0x7FC0u : ((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    uint32_t u = (uint32_t)__bfloat16_as_ushort(v.x) | ((uint32_t)__bfloat16_as_ushort(v.y) << 16);
+    if (lo != lo) u = (u & 0xFFFF0000u) | 0x7FC0u;
+    if (hi != hi) u = (u & 0x0000FFFFu) | 0x7FC00000u;
+    return u;
 }
 
 // ---- launchers (one translation unit each) ---------------------------------

@@ -168,3 +168,69 @@ def test_bf16_error_storage_with_bf16_and_in_kernel_gradients():
     wl = workload.custom("w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
                          fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
     run(wl, 1, 2, error_storage=1)
+
+
+# ---- degenerate values -----------------------------------------------------------
+
+def test_degenerate_values():
+    """Zero, negative-zero, subnormal and constant gradients; an all-zero
+    parameter tensor (trust ratio 1); parameter scales that clip the warmup
+    trust ratio at both bounds; gradients that grow 100x after the freeze so
+    the layerwise factor falls to its lower soft threshold.  Every step is
+    compared with the oracle element by element, and all float state must be
+    bit-identical."""
+    import torch
+    t = [("zero_x", (3000,)), ("zero_g", (5000,)), ("subnormal", (4096,)),
+         ("const", (2055,)), ("negzero", (1000,)), ("tiny_x", (6000,)),
+         ("huge_x", (4100,)), ("grows", (7000,)), ("normal", (9001,))]
+    wl = workload.custom("degenerate", t, W=4, chunk=1024, grad_std=1e-2)
+    off = {n: (int(o), int(o + k)) for (n, _), o, k in zip(t, wl.offsets, wl.numels)}
+    p = Pair(wl)
+    for name, scale in (("zero_x", 0.0), ("tiny_x", 1e-5), ("huge_x", 1e4)):
+        a, b = off[name]
+        p.x[a:b] *= scale
+        p.orc.x[a:b] *= np.float32(scale)
+    assert np.array_equal(p.x.cpu().numpy().view(np.uint32), p.orc.x.view(np.uint32))
+
+    def grads(step, stage):
+        g = workload.grads_for_step(wl, step)
+        a, b = off["zero_g"]; g[:, a:b] = 0.0
+        a, b = off["subnormal"]
+        g[:, a:b] = np.where(g[:, a:b] < 0, -1e-40, 3e-41).astype(np.float32)
+        a, b = off["const"]; g[:, a:b] = 3e-3
+        a, b = off["negzero"]; g[:, a:b] = -0.0
+        if stage == 1:
+            a, b = off["grows"]; g[:, a:b] *= 100.0
+        return g
+
+    def step(kind, stage):
+        g = grads(p.t, stage)
+        dev = torch.from_numpy(g).cuda()
+        if kind == "warmup":
+            p.gpu.warmup_step(dev)
+            p.orc.warmup_step(g)
+        else:
+            p.gpu.compress_step(dev)
+            p.orc.compress_step(g)
+        p.t += 1
+
+    diffs = 0
+    L = {n: i for i, (n, _) in enumerate(t)}
+    for i in range(3):
+        step("warmup", 0)
+        diffs += p.compare(f"warmup {i}")
+        if i == 0:
+            assert p.orc.c_cur[L["zero_x"]] == np.float32(1.0)   # ||x|| = 0: ratio 1
+    c = p.orc.c_cur
+    assert c[L["tiny_x"]] == np.float32(wl.hp["coeff_min"])
+    assert c[L["huge_x"]] == np.float32(wl.hp["coeff_max"])
+    p.freeze()
+    diffs += p.compare("freeze")
+    for i in range(4):
+        step("compress", 1)
+        diffs += p.compare(f"compress {i}")
+    r = p.orc.r_prev
+    # soft threshold: r falls by at most 10 % a step from 1, floor 0.5
+    assert r[L["grows"]] == np.float32(np.float32(np.float32(np.float32(0.9) * np.float32(0.9))
+                                                  * np.float32(0.9)) * np.float32(0.9))
+    assert diffs == 0, f"{diffs} float elements differ in some bit"
