@@ -304,6 +304,49 @@ def test_lossless_compression_reduces_to_frozen_variance_momentum_sgd():
     np.testing.assert_allclose(o.x, x0 - 1e-3 * cvec * u, rtol=1e-6, atol=1e-9)
 
 
+def test_fresh_variance_and_ratio_follow_closed_forms():
+    """Lossless compression for 30 steps: two workers send the same gradient
+    of constant magnitude per chunk, so every chunk compresses exactly (its
+    scale is |z|: a pairwise sum of equal squares over a power-of-two chunk is
+    exact, and sqrt(fl(z^2)) = |z| in binary floating point), the server
+    average of two equal values is exact, and no error is kept.  Then the
+    reconstructed gradient is the true gradient g up to one cancellation, so
+    the fresh second moment solves its recursion in closed form,
+    v_t = beta2^t v0 + (1 - beta2^t) g^2, and the per-tensor ratio is
+    R_t = max over the tensor of (sqrt(v0) + eps) / (sqrt(v_t) + eps).
+    Tensor 0 has two halves with different |g| (the max picks the half whose
+    fresh variance stays smaller); tensor 1's gradient shrinks below the
+    frozen variance, so its ratio rises above 1.  The factor then follows the
+    soft thresholds: r_t = clip(clip(R_t, 0.5, 4), 0.9 r_{t-1}, 1.1 r_{t-1})."""
+    rng = np.random.default_rng(21)
+    numel = [2048, 1024]
+    o = _fresh(numel, 2, 256, HP, x0=rng.standard_normal(3072).astype(np.float32))
+    v0 = np.array([4e-6, 1e-6])
+    mag = np.empty(3072)
+    mag[:1024], mag[1024:2048], mag[2048:] = 4e-3, 2.5e-3, 2e-4    # |g| per element
+    o.v[:2048] = np.float32(v0[0])
+    o.v[2048:] = np.float32(v0[1])
+    o.freeze()
+    sg = np.where(rng.random(3072) < 0.5, -1.0, 1.0)
+    g = np.stack([mag * sg, mag * sg]).astype(np.float32)
+    g32 = np.abs(g[0]).astype(np.float64)
+    b2, eps = 0.999, 1e-6
+    r = np.ones(2)
+    for t in range(1, 31):
+        o.compress_step(g)
+        assert np.all(o.e_w == 0) and np.all(o.e_s == 0), t
+        v_t = np.empty(3072)
+        v_t[:2048] = b2 ** t * v0[0] + (1 - b2 ** t) * g32[:2048] ** 2
+        v_t[2048:] = b2 ** t * v0[1] + (1 - b2 ** t) * g32[2048:] ** 2
+        np.testing.assert_allclose(o.v_fresh, v_t, rtol=2e-5)
+        rho = (np.sqrt(np.repeat(v0, numel)) + eps) / (np.sqrt(v_t) + eps)
+        R = np.array([rho[:2048].max(), rho[2048:].max()])
+        np.testing.assert_allclose(o.R, R, rtol=2e-5)
+        r = np.minimum(np.maximum(np.minimum(np.maximum(R, 0.5), 4.0), 0.9 * r), 1.1 * r)
+        np.testing.assert_allclose(o.r_prev, r, rtol=2e-5)
+    assert o.R[0] < 1.0 < o.R[1]
+
+
 def test_beta2_one_keeps_factor_one_over_steps():
     hp = dict(HP, beta2=1.0)
     rng = np.random.default_rng(10)
