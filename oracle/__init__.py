@@ -63,7 +63,10 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
+        # LAMB1B_ORACLE_LIB: load another build of lamb1b_oracle.c (the
+        # mutation test points it at copies with one planted mistake)
+        alt = os.environ.get("LAMB1B_ORACLE_LIB")
+        L = ctypes.CDLL(alt if alt else build())
         L.orc_cpt_sumsq.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
         L.orc_cpt_sumsq.restype = ctypes.c_float
         L.orc_compress_chunk.argtypes = [_P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64,

@@ -361,6 +361,100 @@ def test_beta2_one_keeps_factor_one_over_steps():
         np.testing.assert_array_equal(o.c_cur, cbar)
 
 
+def _decode(words, scales, N, C):
+    """+-scale per element from packed sign words (bit 1 = +1, LSB first)."""
+    bits = np.unpackbits(np.ascontiguousarray(words).view(np.uint8), bitorder="little")[:N]
+    return np.where(bits == 1, 1.0, -1.0) * np.repeat(np.asarray(scales, np.float64), C)[:N]
+
+
+def test_error_feedback_telescopes_over_full_steps():
+    """Over T compression steps of the full optimizer nothing is held back by
+    either error buffer: for every worker w,
+        sum_t (what w sent) + e_w,T = sum_t (w's momentum before compression),
+    and for the server
+        sum_t (the scattered momentum) + e_s,T = sum_t (average of what the
+        workers sent),
+    where 'sent' is decoded from the exchanged sign words and scales, and a
+    worker's momentum before compression is beta1 m_{t-1} + (1-beta1) g_w,t.
+    Bounds: the binary32 roundings of each step."""
+    rng = np.random.default_rng(23)
+    numel = [1500, 700, 1000]        # N = 3200: a ragged last chunk of 128
+    W, C = 3, 256
+    o = _fresh(numel, W, C, HP, x0=(rng.standard_normal(3200) * 2e-2).astype(np.float32))
+    for _ in range(2):
+        o.warmup_step((rng.standard_normal((W, o.N)) * 1e-2).astype(np.float32))
+    o.freeze()
+    N = o.N
+    sent_w = np.zeros((W, N)); fed_w = np.zeros((W, N))
+    sent_s = np.zeros(N); fed_s = np.zeros(N)
+    tol_w = np.zeros((W, N)); tol_s = np.zeros(N)
+    for t in range(25):
+        g = (rng.standard_normal((W, N)) * 1e-2).astype(np.float32)
+        m_old = o.m.astype(np.float64)
+        o.compress_step(g)
+        dec = np.stack([_decode(o.signs_w[w], o.scale_w[w], N, C) for w in range(W)])
+        mw = 0.9 * m_old + (1 - 0.9) * g.astype(np.float64)
+        sent_w += dec
+        fed_w += mw
+        avg = dec.sum(axis=0) / W
+        sent_s += o.m.astype(np.float64)
+        fed_s += avg
+        # a few roundings per step: the momentum, z = m_w + e, e = z -+ s, and
+        # for the server the sum over workers, the division and y = avg + e_s
+        tol_w += 4 * ulp32(np.abs(mw) + np.abs(dec) + 1e-30)
+        tol_s += 4 * ulp32(np.abs(avg) * W + np.abs(o.m) + 1e-30)
+    assert np.all(np.abs(sent_w + o.e_w - fed_w) <= tol_w)
+    assert np.all(np.abs(sent_s + o.e_s - fed_s) <= tol_s)
+
+
+def test_warmup_coefficient_average_closed_form():
+    """c_bar is the exponential moving average (weight 0.9) of the warmup
+    coefficients, started at the first one.  The first step's ratio clips at
+    coeff_max (huge parameters); the parameters are then made tiny so every
+    later ratio clips at coeff_min:
+        c_bar_T = 0.9^(T-1) coeff_max + (1 - 0.9^(T-1)) coeff_min."""
+    rng = np.random.default_rng(24)
+    o = _fresh([1024], 2, 256, HP, x0=(rng.standard_normal(1024) * 1e3).astype(np.float32))
+    for t in range(1, 9):
+        o.warmup_step((rng.standard_normal((2, 1024)) * 1e-2).astype(np.float32))
+        want_c = 10.0 if t == 1 else 0.01
+        assert o.c_cur[0] == np.float32(want_c), t
+        want_bar = 0.9 ** (t - 1) * 10.0 + (1 - 0.9 ** (t - 1)) * 0.01
+        np.testing.assert_allclose(o.c_bar[0], want_bar, rtol=1e-5)
+        if t == 1:
+            o.x[:] = (rng.standard_normal(1024) * 1e-7).astype(np.float32)
+
+
+def test_compression_update_scales_with_the_layer_factor():
+    """Two optimizers differ only in the soft-threshold width (0.1 and 0.3);
+    the ratio is forced far above factor_max, so the factor rises to 1.1 and
+    1.3 in the first step.  Everything else being equal, their parameter steps
+    differ by exactly that factor (up to rounding): the update is scaled by
+    c = c_bar r, not by c_bar alone.  And the step itself is the frozen-
+    variance preconditioned momentum step (the fresh second moment, here 0,
+    only steers the factor): dx = -lr c_bar r m / (sqrt(v) + eps)."""
+    rng = np.random.default_rng(25)
+    x0 = np.zeros(2048, np.float32)       # steps land exactly on zero parameters
+    g = (rng.standard_normal((2, 2048)) * 1e-9).astype(np.float32)
+    steps = []
+    for thr in (0.1, 0.3):
+        o = _fresh([2048], 2, 256, dict(HP, factor_threshold=thr), x0=x0.copy())
+        o.v[:] = 1e4
+        o.m[:] = np.float32(1e-3)
+        o.c_bar[:] = 0.5
+        o.freeze()
+        o.v_fresh[:] = 0.0
+        o.compress_step(g)
+        np.testing.assert_allclose(o.r_prev, 1.0 + thr, rtol=1e-6)
+        steps.append(o.x.astype(np.float64) - x0.astype(np.float64))
+        # m after the step: 0.9 * 1e-3 + 0.1 g (|g| ~ 1e-9), compressed per chunk
+        want = -1e-3 * 0.5 * (1.0 + thr) * np.abs(o.m.astype(np.float64)) / (100.0 + 1e-6)
+        np.testing.assert_allclose(np.abs(steps[-1]), np.abs(want), rtol=1e-5)
+        np.testing.assert_allclose(np.abs(o.m), 0.9e-3, rtol=1e-5)
+    assert np.all(steps[0] < 0)
+    np.testing.assert_allclose(steps[1] / steps[0], 1.3 / 1.1, rtol=1e-6)
+
+
 def test_soft_threshold_growth_closed_form():
     """With the ratio far above factor_max every step, the factor grows by
     (1 + threshold) per step until it reaches factor_max: r_t =
@@ -477,6 +571,7 @@ def test_adam_variant_lossless_compression_is_frozen_variance_momentum_sgd():
     o = _fresh(numel, 2, 256, HP, x0=rng.standard_normal(3072).astype(np.float32))
     o.variant = 1
     o.v[:] = rng.uniform(1e-6, 1e-4, o.N).astype(np.float32)
+    o.c_bar[:] = 0.5           # a LAMB warmup average, which 1-bit Adam must not use
     o.freeze()
     vf0 = o.v_fresh.copy()
     x0 = o.x.astype(np.float64).copy()
