@@ -88,16 +88,18 @@ def grad_bytes(wl):
 
 
 def fused_kernel_bytes(wl, variant="lamb", errors="f32"):
-    """Algorithmic HBM bytes of one launch of the fused compression kernel:
-    per parameter W*(g + 4 e_w read + 4 e_w written + 1/8 signs) + reads of
-    4 m + 4 e_s + 4 v + 4 v_fresh and writes of 4 e_s + 4 m + 4 v_fresh +
-    1/8 server signs; plus 4 bytes per written scale (W worker + 1 server)."""
+    """Algorithmic HBM bytes of one steady-state launch of the fused
+    compression kernel: per parameter W*(g + 4 e_w read + 4 e_w written + 1/8
+    signs) + the previous step's server signs (1/8, the old momentum) + reads
+    of 4 e_s + 4 v + 4 v_fresh and writes of 4 e_s + 4 v_fresh + 1/8 server
+    signs; plus 4 bytes per scale (W worker scales and the server scale
+    written, the previous server scale read)."""
     W = wl.W
     # 1-bit Adam reads and writes no second moments in this kernel; bfloat16
     # error storage moves 2 + 2 instead of 4 + 4 bytes per error element
     eb = 4.0 if errors == "bf16" else 8.0
-    per = W * (grad_bytes(wl) + eb + 0.125) + (eb + 8.125 + (0.0 if variant == "adam" else 12.0))
-    return wl.N * per + 4.0 * wl.K * (W + 1)
+    per = W * (grad_bytes(wl) + eb + 0.125) + (eb + 0.25 + (0.0 if variant == "adam" else 12.0))
+    return wl.N * per + 4.0 * wl.K * (W + 2)
 
 
 def update_kernel_bytes(wl):

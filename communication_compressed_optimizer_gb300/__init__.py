@@ -191,10 +191,19 @@ class OneBitLamb:
         _abi.check("lamb1b_state_view", self._lib.lamb1b_state_view(self._ctx, ctypes.byref(s)))
         return s
 
-    def state(self) -> dict:
+    def sync_momentum(self, stream=None):
+        """Write the dense momentum m from the last compression step's server
+        sign words and chunk scales (a no-op before the first one)."""
+        _abi.check("lamb1b_sync_momentum",
+                   self._lib.lamb1b_sync_momentum(self._ctx, _stream_handle(stream)))
+
+    def state(self, sync=True) -> dict:
         """Views (not copies) of the state inside the workspace, as torch
-        tensors, plus the counters."""
+        tensors, plus the counters.  sync: first bring the dense momentum
+        up to date (sync_momentum on the current stream)."""
         torch = _torch()
+        if sync:
+            self.sync_momentum()
         s = self.state_raw()
         base = self.workspace.data_ptr()
 

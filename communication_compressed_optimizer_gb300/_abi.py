@@ -20,7 +20,7 @@ GRAD_F32, GRAD_BF16, GRAD_PHILOX = 0, 1, 2
 EXPORTED = ("lamb1b_workspace_bytes", "lamb1b_init", "lamb1b_warmup_step",
             "lamb1b_freeze_variance", "lamb1b_compress_step", "lamb1b_state_view",
             "lamb1b_set_counters", "lamb1b_check_status", "lamb1b_set_trace_events",
-            "lamb1b_set_fault_injection", "lamb1b_destroy",
+            "lamb1b_set_fault_injection", "lamb1b_sync_momentum", "lamb1b_destroy",
             "lamb1b_error_string", "lamb1b_gen_grads", "lamb1b_gen_params",
             "lamb1b_tensor_sumsq_noalloc")
 
@@ -90,6 +90,7 @@ def load(build_if_missing: bool = False):
     L.lamb1b_check_status.argtypes = [_P, _P]
     L.lamb1b_set_trace_events.argtypes = [_P, ctypes.POINTER(_P), i32]
     L.lamb1b_set_fault_injection.argtypes = [_P, i32, ctypes.c_uint32]
+    L.lamb1b_sync_momentum.argtypes = [_P, _P]
     L.lamb1b_destroy.argtypes = [_P]
     L.lamb1b_error_string.argtypes = [ctypes.c_int]
     L.lamb1b_error_string.restype = ctypes.c_char_p

@@ -10,13 +10,16 @@
 //
 // Data movement: CTAs are persistent (tile t = blockIdx.x + i*gridDim.x; a
 // tile is 4096 elements = 4096/C chunks, or one 8192-element chunk).
-// Every input of a tile -- the old momentum, each worker's gradient and
-// error, then the server error, frozen and fresh second moments -- is copied
-// into a 7-slot ring of shared-memory slots by TMA bulk copies
-// (cp.async.bulk, completion on one mbarrier per slot), issued by thread 0 as
-// soon as enough slots are released, so the next arrays stream in while the
-// CTA reduces and stores the current one; while the server phase holds its
-// three arrays the next tile's momentum and first worker are already loading.  Outputs are written with coalesced 16-byte stores.
+// Every input of a tile -- the old momentum (after the first compression
+// step: the last server message, sign words and chunk scales, 1/32 of the
+// bytes; m is exactly sign x scale, so no dense copy is kept), each worker's
+// gradient and error, then the server error, frozen and fresh second
+// moments -- is copied into a 7-slot ring of shared-memory slots by TMA bulk
+// copies (cp.async.bulk, completion on one mbarrier per slot), issued by
+// thread 0 as soon as enough slots are released, so the next arrays stream
+// in while the CTA reduces and stores the current one; while the server phase
+// holds its three arrays the next tile's momentum and first worker are
+// already loading.  Outputs are written with coalesced 16-byte stores.
 //
 // Thread map: thread `tid` of an NT-thread CTA holds SLOTS aligned float4
 // groups, group s at chunk offset s*NT*4 + tid*4.  Warp w's lanes therefore
@@ -177,7 +180,21 @@ __device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, i
         tma::load(ring + (uint32_t)sl * R::kSlot, src, bytes, &full[sl]);
     };
     if (r == 0) {
-        copy(0, D.m + base, R::kSlot);
+        if (P.m_packed) {
+            // the tile's server sign words, then the 16-byte-aligned span of
+            // chunk scales that holds its chunks (scale_s is padded by 16)
+            if (pos == P.skip_copy && blockIdx.x == 0) return;
+            const int64_t k0 = base >> P.log2c;
+            const int64_t ka = k0 & ~int64_t(3);
+            const uint32_t nsc = (uint32_t)(k0 - ka) + (uint32_t)(TILE >> P.log2c);
+            const uint32_t sbytes = (nsc * 4u + 15u) / 16u * 16u;
+            const int sl = p.slot;
+            tma::arrive_expect_tx(&full[sl], TILE / 8 + sbytes);
+            tma::load(ring + (uint32_t)sl * R::kSlot, D.signs_s + base / 32, TILE / 8, &full[sl]);
+            tma::load(ring + (uint32_t)sl * R::kSlot + TILE / 8, D.scale_s + ka, sbytes, &full[sl]);
+        } else {
+            copy(0, D.m + base, R::kSlot);
+        }
     } else if (r <= W) {
         const int w = r - 1;
         if constexpr (SG > 0) {
@@ -402,19 +419,36 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
         }
 
         // ---- item M: beta1 * m_old, kept for the whole tile ------------------
+        // m_old is the dense momentum after the warmup, afterwards the last
+        // step's server signs times its chunk scales (exactly the same values)
         float bm[SLOTS][4], acc[SLOTS][4];
         {
             if (!wait_slots<NSLOT>(full, cp, 1, P.wait_tries)) lost = true;
-            const float* a = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
+            const unsigned char* a = ring + (uint32_t)cp.slot * R::kSlot;
             cp = cp.plus(1);
+            if (P.m_packed) {
+                const uint32_t* words = reinterpret_cast<const uint32_t*>(a);
+                const float* scales = reinterpret_cast<const float*>(a + TILE / 8) + (k0 & 3);
 #pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const float4 mo = *reinterpret_cast<const float4*>(a + s * NT * 4 + tid * 4);
-                bm[s][0] = fmul(P.beta1, mo.x); bm[s][1] = fmul(P.beta1, mo.y);
-                bm[s][2] = fmul(P.beta1, mo.z); bm[s][3] = fmul(P.beta1, mo.w);
+                for (int s = 0; s < SLOTS; ++s) {
+                    const int e0 = s * NT * 4 + tid * 4;
+                    const uint32_t bits = words[e0 >> 5] >> (e0 & 31);
+                    const float sc = scales[e0 / C];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) bm[s][c] = fmul(P.beta1, ((bits >> c) & 1u) ? sc : -sc);
+                }
+            } else {
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    const float4 mo = *reinterpret_cast<const float4*>(a + (s * NT * 4 + tid * 4) * 4);
+                    bm[s][0] = fmul(P.beta1, mo.x); bm[s][1] = fmul(P.beta1, mo.y);
+                    bm[s][2] = fmul(P.beta1, mo.z); bm[s][3] = fmul(P.beta1, mo.w);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[s][c] = 0.0f;
-            }
         }
 
         // ---- phase 1: every worker compresses its chunks ----------------------
@@ -627,7 +661,6 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                         }
                     }
                     store_err4<EB>(D.e_s, base + off, es);
-                    *reinterpret_cast<float4*>(D.m + base + off) = make_float4(mn[0], mn[1], mn[2], mn[3]);
                     if constexpr (!ADAM)
                         *reinterpret_cast<float4*>(D.v_fresh + base + off) =
                             make_float4(vf[0], vf[1], vf[2], vf[3]);

@@ -110,6 +110,32 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
     }
 }
 
+// ---- dense momentum from the server's sign words and chunk scales ---------
+// m[i] = sign_i x scale_k for i < N (elements >= N stay 0): the values a
+// compression step leaves in m, written out for inspection and checkpoints.
+__global__ void __launch_bounds__(kNT) k_unpack_momentum(const Problem P, const Dev D)
+{
+    const int64_t b0 = (int64_t)blockIdx.x * kBlock;
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+        const int64_t idx = b0 + s * kNT * 4 + threadIdx.x * 4;
+        if (idx >= P.N) break;
+        float mm[4];
+        update_momentum4(P, D, 1, idx, mm);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (idx + c >= P.N) mm[c] = 0.0f;
+        *reinterpret_cast<float4*>(D.m + idx) = make_float4(mm[0], mm[1], mm[2], mm[3]);
+    }
+}
+
+cudaError_t launch_unpack_momentum(const Problem& P, const Dev& D, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)((P.N + kBlock - 1) / kBlock);
+    k_unpack_momentum<<<grid, kNT, 0, st>>>(P, D);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st)
 {
     const unsigned grid = (unsigned)((P.N + kBlock - 1) / kBlock);

@@ -351,6 +351,9 @@ extern "C" int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, 
     if (rc) return rc;
     if ((rc = grads_check(ctx, grads))) return rc;
     const Grads G = to_grads(ctx, grads);
+    // after the first compression step m lives in the server's sign words
+    // and chunk scales; before it, in the dense buffer the warmup left
+    ctx->P.m_packed = ctx->t > ctx->n_warm ? 1 : 0;
     NvtxRange range("lamb1b compression step");
     if (lamb1b::launch_compress(ctx->P, ctx->D, G, ctx->x, static_cast<cudaStream_t>(stream),
                                 ctx->tracing ? ctx->ev : nullptr) != cudaSuccess)
@@ -418,6 +421,18 @@ extern "C" int lamb1b_set_trace_events(lamb1b_ctx* ctx, void* const* events, int
     }
     for (int i = 0; i < 4; ++i) ctx->ev[i] = static_cast<cudaEvent_t>(events[i]);
     ctx->tracing = true;
+    return LAMB1B_OK;
+}
+
+extern "C" int lamb1b_sync_momentum(lamb1b_ctx* ctx, void* stream)
+{
+    if (!ctx) return LAMB1B_ERR_ARG;
+    if (!(ctx->stage == 1 && ctx->t > ctx->n_warm)) return LAMB1B_OK;   // m is dense
+    int rc = device_check(ctx);
+    if (rc) return rc;
+    NvtxRange range("lamb1b sync momentum");
+    if (lamb1b::launch_unpack_momentum(ctx->P, ctx->D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LAMB1B_ERR_CUDA;
     return LAMB1B_OK;
 }
 

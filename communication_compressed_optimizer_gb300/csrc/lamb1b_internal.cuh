@@ -34,6 +34,8 @@ struct Problem {
     int32_t log2c;      // C = 2^log2c
     int32_t w_pow2;     // W is a power of two
     float inv_w;        // 1 / W (exact when w_pow2)
+    int32_t m_packed;    // compression stage after its first step: m is held as the
+                         // server's sign words and chunk scales (signs_s, scale_s)
     uint32_t wait_tries; // bound of every shared-memory copy wait (try_wait calls)
     int32_t skip_copy;   // fault injection: copy position left out by CTA 0, or -1
 };
@@ -168,6 +170,7 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi)
 cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float* x,
                           cudaStream_t st, int first_warmup, const cudaEvent_t* ev);
 cudaError_t launch_freeze(const Problem& P, const Dev& D, cudaStream_t st);
+cudaError_t launch_unpack_momentum(const Problem& P, const Dev& D, cudaStream_t st);
 cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
                             cudaStream_t st, const cudaEvent_t* ev);
 

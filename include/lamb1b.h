@@ -128,7 +128,14 @@ typedef struct {
 
 /* Device views of the optimizer state inside the workspace (for inspection,
  * checkpointing and restore; the caller may read or overwrite them between
- * calls).  Padded layouts: Np = N rounded up to a multiple of max(C, 4096)
+ * calls).  The momentum: after a compression step m is exactly the server's
+ * sign times its chunk scale, and the library keeps it in that form only
+ * (signs_s, scale_s, 1/32 of the bytes): the dense m is current in the warmup
+ * stage and right after the freeze, and after a compression step only once
+ * lamb1b_sync_momentum has written it.  From the first compression step on,
+ * signs_s and scale_s are the momentum a later step reads; a restore must
+ * write them (the counters passed to lamb1b_set_counters tell the library
+ * which form is current: t > n_warmup in the compression stage).  Padded layouts: Np = N rounded up to a multiple of max(C, 4096)
  * elements per vector (>= K*C), words_ld = Np/32.
  *   m, v, v_fresh: [Np] binary32; elements >= N are kept at 0
  *   e_s: [Np], e_w: [W][Np], binary32 or (error_storage = 1) bfloat16 bits
@@ -233,6 +240,13 @@ int lamb1b_check_status(lamb1b_ctx* ctx, void* stream);
  * and must stay valid while tracing is on.  n == 0 turns tracing off.
  * Errors: ARG for other n or NULL events with n == 4. */
 int lamb1b_set_trace_events(lamb1b_ctx* ctx, void* const* events, int32_t n);
+
+/* Writes the dense momentum m (lamb1b_state.m) from the server sign words and
+ * chunk scales of the last compression step, on `stream`; a no-op while the
+ * dense m is current (warmup stage, and the compression stage before its
+ * first step).  Elements >= N stay 0.
+ * Errors: ARG for a NULL ctx; DEVICE, CUDA as for the steps. */
+int lamb1b_sync_momentum(lamb1b_ctx* ctx, void* stream);
 
 /* Testing hook for the failure path of the compression step (the paper has
  * no counterpart).  The compression kernel stages its inputs through shared

@@ -25,8 +25,8 @@ from harness import SCALAR_TOL, close_scalar, layers_of
 
 pytestmark = pytest.mark.gpu
 
-SEEDS = dict(m=101, v=102, v_fresh=103, e_s=104, e_w=1000)
-STDS = dict(m=1e-3, v=1e-3, v_fresh=1e-3, e_s=1e-4, e_w=1e-4)
+SEEDS = dict(m=101, v=102, v_fresh=103, e_s=104, e_w=1000, signs=105, scales=106)
+STDS = dict(m=1e-3, v=1e-3, v_fresh=1e-3, e_s=1e-4, e_w=1e-4, signs=1.0, scales=1e-3)
 STEP = 10
 
 
@@ -99,8 +99,14 @@ def test_full_size_compression_step_sampled(name):
     opt = pkg.OneBitLamb(x, layers_of(wl), W, C, **wl.hp)
     opt.freeze_variance()
     st = opt.state()
-    for k in ("m", "v", "v_fresh", "e_s"):
+    for k in ("v", "v_fresh", "e_s"):
         pkg.gen_params(st[k], 0, N, STDS[k], SEEDS[k])
+    # mid-training momentum: the last step's server message, in the packed
+    # form a compression step keeps (random sign words, positive chunk scales)
+    nwords = -(-N // 32)
+    pkg.gen_params(st["signs_s"].view(torch.float32), 0, nwords, STDS["signs"], SEEDS["signs"])
+    pkg.gen_params(st["scale_s"], 0, K, STDS["scales"], SEEDS["scales"])
+    st["scale_s"][:K].abs_()
     st["v"][:N].mul_(st["v"][:N])
     st["v_fresh"][:N].mul_(st["v_fresh"][:N])
     for w in range(W):
@@ -132,7 +138,13 @@ def test_full_size_compression_step_sampled(name):
 
     x0 = gather_host(lambda lo, hi: host_normal(wl.seed, wl.param_std, lo, hi))
     o = oracle.Oracle([f[1] for f in frags], [f[2] for f in frags], W, C, wl.hp, x0)
-    o.m[:] = gather_host(lambda lo, hi: host_normal(SEEDS["m"], STDS["m"], lo, hi))
+    def packed_m(lo, hi):
+        q0, q1 = lo // 32, -(-hi // 32)
+        words = host_normal(SEEDS["signs"], STDS["signs"], q0, q1).view(np.uint32)
+        bits = np.unpackbits(words.view(np.uint8), bitorder="little")[lo - q0 * 32:hi - q0 * 32]
+        sc = np.abs(host_normal(SEEDS["scales"], STDS["scales"], lo // C, lo // C + 1))[0]
+        return np.where(bits == 1, sc, -sc).astype(np.float32)
+    o.m[:] = gather_host(packed_m)
     v = gather_host(lambda lo, hi: host_normal(SEEDS["v"], STDS["v"], lo, hi))
     o.v[:] = v * v
     vf = gather_host(lambda lo, hi: host_normal(SEEDS["v_fresh"], STDS["v_fresh"], lo, hi))

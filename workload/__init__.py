@@ -295,9 +295,3 @@ def grads_for_step(wl: Workload, t: int, ld: int | None = None) -> np.ndarray:
         else:
             g[w, :wl.N] = gen_grads(wl, t, w)
     return g
-
-
-def alg_bytes_per_param(W: int, grad_bytes: float) -> float:
-    """Algorithmic HBM bytes per parameter of one compression step of the
-    fused design (worker+server pass plus the update pass)."""
-    return W * (grad_bytes + 8.125) + 44.125
