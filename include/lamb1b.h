@@ -216,7 +216,11 @@ int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream);
  *              (1-factor_threshold) r_prev_l, (1+factor_threshold) r_prev_l)
  *   c_l = c_bar_l r_l;  m = m_new;  x = x - (lr c_l)(m / (sqrt(v)+eps) + wd x)
  * The packed words and scales of every worker and of the server are left in
- * the workspace (lamb1b_state_view).  Errors: STATE before the freeze. */
+ * the workspace (lamb1b_state_view); the new m is kept as the server's words
+ * and scales (signs_s, scale_s) and written densely only by
+ * lamb1b_sync_momentum.  Enqueues kernels only (no host synchronisation, no
+ * allocation), so a step can be captured in a CUDA graph; the host step
+ * counter advances on direct calls.  Errors: STATE before the freeze. */
 int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, void* stream);
 
 /* Fills *out with device pointers into the workspace and the counters. */

@@ -29,7 +29,10 @@ def _rank(rank, world, port, out):
     bench.barrier(w)
     # rank r "took" 1 + r seconds for 1000 units
     value, slowest = bench.aggregate_throughput(1.0 + rank, 1000, w)
-    out.put((rank, value, slowest))
+    # the end-to-end leg runs only where every rank's host buffer fits: one
+    # rank that does not fit makes all of them skip it
+    any_short = bench.max_over_ranks(1.0 if rank == 1 else 0.0, w)
+    out.put((rank, value, slowest, any_short))
     bench.barrier(w)
     import torch.distributed as dist
     dist.destroy_process_group()
@@ -46,12 +49,20 @@ def test_two_gloo_ranks_report_whole_job_throughput():
         p.join(120)
         assert p.exitcode == 0
     res = sorted(out.get(timeout=10) for _ in range(2))
-    for rank, value, slowest in res:
+    for rank, value, slowest, any_short in res:
         assert slowest == pytest.approx(2.0)          # the slower rank's time
         assert value == pytest.approx(2 * 1000 / 2.0)  # all units / slowest time
+        assert any_short == 1.0
 
 
 def test_single_rank_needs_no_process_group():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.aggregate_throughput(2.0, 100, 1) == (50.0, 2.0)
+
+
+def test_host_memory_is_read_for_the_end_to_end_guard():
+    sys.path.insert(0, ROOT)
+    import bench
+    avail = bench.host_memory_available()
+    assert avail is None or avail > 0
