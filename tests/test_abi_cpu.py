@@ -108,6 +108,7 @@ def test_null_context_calls():
     assert L.lamb1b_set_counters(None, 0, 0, 0) == _abi.ERR_ARG
     assert L.lamb1b_check_status(None, None) == _abi.ERR_ARG
     assert L.lamb1b_set_fault_injection(None, -1, 0) == _abi.ERR_ARG
+    assert L.lamb1b_sync_momentum(None, None) == _abi.ERR_ARG
     assert L.lamb1b_destroy(None) == 0
     for code in range(0, -9, -1):
         assert L.lamb1b_error_string(code)
