@@ -13,8 +13,8 @@
 // Every input of a tile -- the old momentum (after the first compression
 // step: the last server message, sign words and chunk scales, 1/32 of the
 // bytes; m is exactly sign x scale, so no dense copy is kept), each worker's
-// gradient and error, then the server error, frozen and fresh second
-// moments -- is copied into a 7-slot ring of shared-memory slots by TMA bulk
+// gradient and error, then the server error, the frozen preconditioner
+// sqrt(v) + eps and the fresh second moment -- is copied into a 7-slot ring of shared-memory slots by TMA bulk
 // copies (cp.async.bulk, completion on one mbarrier per slot), issued by
 // thread 0 as soon as enough slots are released, so the next arrays stream
 // in while the CTA reduces and stores the current one; while the server phase
@@ -125,9 +125,10 @@ template <int GK>
 struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGradBF16 ? 2 : 0); };
 
 // Ring of NSLOT shared-memory slots of TILE floats, one mbarrier per slot.
-// Every tile streams, in slot positions: M (m_old), then per worker W_w its
-// gradients (when stored) and its error, then S (e_s, and v for 1-bit LAMB),
-// then F (v_fresh, 1-bit LAMB only).  Slot position p lives in slot p % NSLOT
+// Every tile streams, in slot positions: M (m_old, dense or as the last
+// server message), then per worker W_w its gradients (when stored) and its
+// error, then S (e_s, and for 1-bit LAMB the frozen sqrt(v) + eps), then F
+// (v_fresh, 1-bit LAMB only).  Slot position p lives in slot p % NSLOT
 // and completes phase (p / NSLOT) of that slot's barrier.
 template <int TILE>
 struct Ring {
@@ -207,7 +208,7 @@ __device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, i
         }
     } else if (r == W + 1) {
         copy(0, es + base * esz, kErrBytes);
-        if constexpr (!ADAM) copy(1, D.v + base, R::kSlot);
+        if constexpr (!ADAM) copy(1, D.d_frz + base, R::kSlot);
     } else {
         copy(0, D.v_fresh + base, R::kSlot);
     }
@@ -571,10 +572,10 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             const int nsrv = SL::kServer + (ADAM ? 0 : 1);      // S (and F) slots
             if (!wait_slots<NSLOT>(full, cp, nsrv, P.wait_tries)) lost = true;
             const float* es_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.slot * R::kSlot);
-            const float* v_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(1).slot * R::kSlot);
+            const float* d_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(1).slot * R::kSlot);
             const float* vf_in = reinterpret_cast<const float*>(ring + (uint32_t)cp.plus(2).slot * R::kSlot);
             cp = cp.plus(nsrv);
-            float y[SLOTS][4], vz[SLOTS][4], vfo[SLOTS][4];
+            float y[SLOTS][4], dz[SLOTS][4], vfo[SLOTS][4];
             auto average_and_norms = [&](auto full_c) {
                 constexpr bool FULL = decltype(full_c)::value;
                 float part[SLOTS];
@@ -584,9 +585,9 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                     float ee[4];
                     load_err4<EB>(es_in, off, ee);
                     if constexpr (!ADAM) {
-                        const float4 v = *reinterpret_cast<const float4*>(v_in + off);
+                        const float4 v = *reinterpret_cast<const float4*>(d_in + off);
                         const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
-                        vz[s][0] = v.x; vz[s][1] = v.y; vz[s][2] = v.z; vz[s][3] = v.w;
+                        dz[s][0] = v.x; dz[s][1] = v.y; dz[s][2] = v.z; dz[s][3] = v.w;
                         vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
                     }
 #pragma unroll
@@ -646,7 +647,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                         const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
                         vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
                         if (valid) {
-                            float rho = fdiv(fadd(fsqrt(vz[s][c]), P.eps), fadd(fsqrt(vf[c]), P.eps));
+                            float rho = fdiv(dz[s][c], fadd(fsqrt(vf[c]), P.eps));
                             if (rho != rho) rho = __int_as_float(0x7F800000);
                             if constexpr (!ONE) {
                                 const int64_t i = base + off + c;

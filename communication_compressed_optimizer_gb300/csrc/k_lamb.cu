@@ -35,9 +35,25 @@ __device__ __forceinline__ void update_momentum4(const Problem& P, const Dev& D,
     }
 }
 
+// The preconditioner fl(sqrt(v) + eps) of 4 elements at idx: precomputed from
+// the frozen v in the compression stage (msig), else formed from v.
+__device__ __forceinline__ void update_denominator4(const Problem& P, const Dev& D, int msig, int64_t idx,
+                                                    float d[4])
+{
+    if (msig) {
+        const float4 d4 = *reinterpret_cast<const float4*>(D.d_frz + idx);
+        d[0] = d4.x; d[1] = d4.y; d[2] = d4.z; d[3] = d4.w;
+    } else {
+        const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
+        d[0] = fadd(fsqrt(v4.x), P.eps); d[1] = fadd(fsqrt(v4.y), P.eps);
+        d[2] = fadd(fsqrt(v4.z), P.eps); d[3] = fadd(fsqrt(v4.w), P.eps);
+    }
+}
+
 // ---- update: x = x - (lr c_l) (m / (sqrt(v) + eps) + wd x) ----------------
 // Warmup: m, v are this step's moments.  Compression stage: m is the
-// decompressed server momentum and v the frozen second moment.
+// decompressed server momentum and v the frozen second moment, whose
+// sqrt(v) + eps is precomputed (d_frz).
 // msig: m is the decompressed server momentum of this step, read from its sign
 // words and chunk scales (1/32 of the bytes) instead of the dense copy.
 __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, float* __restrict__ x,
@@ -51,22 +67,20 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
     if (b0 + kBlock <= P.N && lend >= b0 + kBlock) {
         // the whole block lies in tensor l: every load is issued before any
         // arithmetic or store
-        float mm[kSlots][4], vv[kSlots][4], xv[kSlots][4];
+        float mm[kSlots][4], dd[kSlots][4], xv[kSlots][4];
 #pragma unroll
         for (int s = 0; s < kSlots; ++s) {
             const int64_t idx = b0 + s * kNT * 4 + tid * 4;
             update_momentum4(P, D, msig, idx, mm[s]);
-            const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
+            update_denominator4(P, D, msig, idx, dd[s]);
             const float4 x4 = *reinterpret_cast<const float4*>(x + idx);
-            vv[s][0] = v4.x; vv[s][1] = v4.y; vv[s][2] = v4.z; vv[s][3] = v4.w;
             xv[s][0] = x4.x; xv[s][1] = x4.y; xv[s][2] = x4.z; xv[s][3] = x4.w;
         }
 #pragma unroll
         for (int s = 0; s < kSlots; ++s) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const float d = fadd(fsqrt(vv[s][c]), P.eps);
-                const float u = fadd(fdiv(mm[s][c], d), fmul(P.wd, xv[s][c]));
+                const float u = fadd(fdiv(mm[s][c], dd[s][c]), fmul(P.wd, xv[s][c]));
                 xv[s][c] = fsub(xv[s][c], fmul(gcl, u));
             }
             *reinterpret_cast<float4*>(x + b0 + s * kNT * 4 + tid * 4) =
@@ -80,8 +94,8 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
         if (idx >= P.N) break;
         float mm[4];
         update_momentum4(P, D, msig, idx, mm);
-        const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
-        const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+        float dd[4];
+        update_denominator4(P, D, msig, idx, dd);
         const bool full = idx + 4 <= P.N;
         float xv[4];
         if (full) {
@@ -96,8 +110,7 @@ __global__ void __launch_bounds__(kNT) k_update(const Problem P, const Dev D, fl
             const int64_t i = idx + c;
             if (i < P.N) {
                 while (i >= lend) { ++l; lend = D.layer_end[l]; gcl = D.gc[l]; }
-                const float d = fadd(fsqrt(vv[c]), P.eps);
-                const float u = fadd(fdiv(mm[c], d), fmul(P.wd, xv[c]));
+                const float u = fadd(fdiv(mm[c], dd[c]), fmul(P.wd, xv[c]));
                 xv[c] = fsub(xv[c], fmul(gcl, u));
             }
         }
@@ -133,6 +146,27 @@ cudaError_t launch_unpack_momentum(const Problem& P, const Dev& D, cudaStream_t 
 {
     const unsigned grid = (unsigned)((P.N + kBlock - 1) / kBlock);
     k_unpack_momentum<<<grid, kNT, 0, st>>>(P, D);
+    return cudaGetLastError();
+}
+
+// ---- the frozen preconditioner: d = fl(fl(sqrt(v)) + eps) over [0, Np) -----
+// v does not change in the compression stage, so both compression-stage
+// kernels read d instead of recomputing it (same bits, one square root and
+// one addition less per element and step).
+__global__ void __launch_bounds__(kNT) k_frozen_denominator(const Problem P, const Dev D)
+{
+    const int64_t idx = ((int64_t)blockIdx.x * kNT + threadIdx.x) * 4;
+    if (idx >= P.Np) return;
+    const float4 v4 = *reinterpret_cast<const float4*>(D.v + idx);
+    *reinterpret_cast<float4*>(D.d_frz + idx) =
+        make_float4(fadd(fsqrt(v4.x), P.eps), fadd(fsqrt(v4.y), P.eps),
+                    fadd(fsqrt(v4.z), P.eps), fadd(fsqrt(v4.w), P.eps));
+}
+
+cudaError_t launch_frozen_denominator(const Problem& P, const Dev& D, cudaStream_t st)
+{
+    const unsigned grid = (unsigned)((P.Np / 4 + kNT - 1) / kNT);
+    k_frozen_denominator<<<grid, kNT, 0, st>>>(P, D);
     return cudaGetLastError();
 }
 
@@ -381,7 +415,8 @@ cudaError_t launch_freeze(const Problem& P, const Dev& D, cudaStream_t st)
     if ((e = cudaMemsetAsync(D.e_w, 0, fe * P.Np * P.W, st))) return e;
     if ((e = cudaMemsetAsync(D.e_s, 0, fe * P.Np, st))) return e;
     k_layers_reset<<<(P.L + 255) / 256, 256, 0, st>>>(P, D, 0);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError())) return e;
+    return launch_frozen_denominator(P, D, st);
 }
 
 cudaError_t launch_init_layers(const Problem& P, const Dev& D, cudaStream_t st)

@@ -19,7 +19,7 @@ using lamb1b::Problem;
 namespace {
 
 enum Region {
-    R_M, R_V, R_VF, R_ES, R_EW, R_SW, R_SS, R_SCW, R_SCS,
+    R_M, R_V, R_VF, R_DF, R_ES, R_EW, R_SW, R_SS, R_SCW, R_SCS,
     R_CBAR, R_RPREV, R_CCUR, R_GC, R_RLAST, R_SX, R_SU, R_RMAX,
     R_LOFF, R_LEND, R_HBASE, R_CL0, R_CL1, R_PX, R_PU, R_FLAGS, R_COUNT
 };
@@ -83,7 +83,7 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     const size_t f = sizeof(float);
     size_t bytes[R_COUNT];
     const size_t fe = hp->error_storage ? 2 : 4;   // error element size
-    bytes[R_M] = bytes[R_V] = bytes[R_VF] = f * p->Np;
+    bytes[R_M] = bytes[R_V] = bytes[R_VF] = bytes[R_DF] = f * p->Np;
     bytes[R_ES] = fe * p->Np;
     bytes[R_EW] = fe * p->Np * p->W;
     bytes[R_SW] = sizeof(uint32_t) * p->words_ld * p->W;
@@ -127,6 +127,7 @@ struct lamb1b_ctx {
     std::vector<int64_t> off, end, hbase;
     std::vector<int32_t> l0, l1;
     bool tracing = false;
+    bool d_frz_valid = false;   // D.d_frz holds sqrt(v) + eps of the frozen v
     cudaEvent_t ev[4] = {};
 };
 
@@ -242,6 +243,7 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     D.m = reinterpret_cast<float*>(ws + p.off[R_M]);
     D.v = reinterpret_cast<float*>(ws + p.off[R_V]);
     D.v_fresh = reinterpret_cast<float*>(ws + p.off[R_VF]);
+    D.d_frz = reinterpret_cast<float*>(ws + p.off[R_DF]);
     D.e_s = reinterpret_cast<float*>(ws + p.off[R_ES]);
     D.e_w = reinterpret_cast<float*>(ws + p.off[R_EW]);
     D.signs_w = reinterpret_cast<uint32_t*>(ws + p.off[R_SW]);
@@ -340,6 +342,7 @@ extern "C" int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream)
     if (lamb1b::launch_freeze(ctx->P, ctx->D, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
     ctx->stage = 1;
+    ctx->d_frz_valid = true;
     return LAMB1B_OK;
 }
 
@@ -355,6 +358,12 @@ extern "C" int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, 
     // and chunk scales; before it, in the dense buffer the warmup left
     ctx->P.m_packed = ctx->t > ctx->n_warm ? 1 : 0;
     NvtxRange range("lamb1b compression step");
+    if (!ctx->d_frz_valid) {     // after a restore: rebuild sqrt(v) + eps of the frozen v
+        if (lamb1b::launch_frozen_denominator(ctx->P, ctx->D, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+            return LAMB1B_ERR_CUDA;
+        ctx->d_frz_valid = true;
+    }
     if (lamb1b::launch_compress(ctx->P, ctx->D, G, ctx->x, static_cast<cudaStream_t>(stream),
                                 ctx->tracing ? ctx->ev : nullptr) != cudaSuccess)
         return LAMB1B_ERR_CUDA;
@@ -386,6 +395,7 @@ extern "C" int lamb1b_set_counters(lamb1b_ctx* ctx, int64_t t, int32_t n_warmup,
     ctx->t = t;
     ctx->n_warm = n_warmup;
     ctx->stage = stage;
+    ctx->d_frz_valid = false;    // v may have been rewritten: rebuilt before the next step
     return LAMB1B_OK;
 }
 

@@ -45,6 +45,7 @@ struct Dev {
     float* m;         // [Np]
     float* v;         // [Np]  second moment; frozen after the stage switch
     float* v_fresh;   // [Np]
+    float* d_frz;     // [Np]  fl(sqrt(v) + eps) of the frozen v (compression stage)
     float* e_s;       // [Np]     binary32, or bfloat16 bits when P.ebf16
     float* e_w;       // [W][Np]  binary32, or bfloat16 bits when P.ebf16
     uint32_t* signs_w;// [W][words_ld]
@@ -171,6 +172,7 @@ cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float*
                           cudaStream_t st, int first_warmup, const cudaEvent_t* ev);
 cudaError_t launch_freeze(const Problem& P, const Dev& D, cudaStream_t st);
 cudaError_t launch_unpack_momentum(const Problem& P, const Dev& D, cudaStream_t st);
+cudaError_t launch_frozen_denominator(const Problem& P, const Dev& D, cudaStream_t st);
 cudaError_t launch_compress(const Problem& P, const Dev& D, const Grads& G, float* x,
                             cudaStream_t st, const cudaEvent_t* ev);
 

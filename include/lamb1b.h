@@ -135,7 +135,10 @@ typedef struct {
  * lamb1b_sync_momentum has written it.  From the first compression step on,
  * signs_s and scale_s are the momentum a later step reads; a restore must
  * write them (the counters passed to lamb1b_set_counters tell the library
- * which form is current: t > n_warmup in the compression stage).  Padded layouts: Np = N rounded up to a multiple of max(C, 4096)
+ * which form is current: t > n_warmup in the compression stage).  Likewise v
+ * is frozen in the compression stage and the library keeps fl(sqrt(v) + eps)
+ * precomputed from it; after rewriting v, call lamb1b_set_counters (as every
+ * restore does) and the next step rebuilds it.  Padded layouts: Np = N rounded up to a multiple of max(C, 4096)
  * elements per vector (>= K*C), words_ld = Np/32.
  *   m, v, v_fresh: [Np] binary32; elements >= N are kept at 0
  *   e_s: [Np], e_w: [W][Np], binary32 or (error_storage = 1) bfloat16 bits
