@@ -227,30 +227,37 @@ __device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int
 }
 
 // Chunk totals from the tile's 128-leaf partials red[0 .. NPART) (element
-// order).  Lane j returns the canonical sum of squares of chunk j / LPC of
-// the tile, LPC = lanes per chunk: the first log2(LPC) butterfly stages are
-// exactly the pairwise tree over each chunk's partials.
+// order).  Each lane loads G = min(4, PPC) consecutive partials with one
+// vector load and adds them as the canonical tree does (the level-2 subtrees
+// of a chunk's tree); the remaining log2(LPC) butterfly stages, LPC = PPC / G
+// lanes per chunk, finish each chunk's tree.  Lanes past LUSED = NPART / G
+// repeat lanes lane % LUSED, so every lane returns the total of chunk
+// (lane % LUSED) / LPC of the tile.
+template <int NPART, int PPC>
+struct ChunkLanes {
+    static constexpr int G = PPC >= 4 ? 4 : PPC;     // partials per lane
+    static constexpr int LPC = PPC / G;              // lanes per chunk
+    static constexpr int LUSED = NPART / G;          // lanes with distinct partials
+    static_assert(PPC % G == 0 && LUSED >= 1 && LUSED <= 32, "chunk / tile shape");
+};
+
 template <int NPART, int PPC>
 __device__ __forceinline__ float chunk_totals(const float* red, int lane)
 {
-    constexpr int PER = NPART > 32 ? NPART / 32 : 1;
-    constexpr int LPC = PPC / PER;
-    static_assert(PPC % PER == 0 && LPC >= 1 && LPC <= 32, "chunk / tile shape");
+    using CL = ChunkLanes<NPART, PPC>;
+    const float* r = red + (lane % CL::LUSED) * CL::G;
     float v;
-    if constexpr (PER == 1) {
-        v = (lane < NPART) ? red[lane] : 0.0f;
+    if constexpr (CL::G == 4) {
+        const float4 q = *reinterpret_cast<const float4*>(r);
+        v = fadd(fadd(q.x, q.y), fadd(q.z, q.w));
+    } else if constexpr (CL::G == 2) {
+        const float2 q = *reinterpret_cast<const float2*>(r);
+        v = fadd(q.x, q.y);
     } else {
-        float t[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) t[j] = red[lane * PER + j];
-#pragma unroll
-        for (int w = 1; w < PER; w <<= 1)
-#pragma unroll
-            for (int j = 0; j < PER; j += 2 * w) t[j] = fadd(t[j], t[j + w]);
-        v = t[0];
+        v = r[0];
     }
 #pragma unroll
-    for (int o = 1; o < LPC; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    for (int o = 1; o < CL::LPC; o <<= 1) v = fadd(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
 
@@ -317,8 +324,8 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
     constexpr int TILE = NT * 4 * SLOTS;
     constexpr int NPART = TILE / 128;           // 128-leaf partials per tile
     constexpr int PPC = C / 128;                // partials per chunk
-    constexpr int PER = NPART > 32 ? NPART / 32 : 1;
-    constexpr int LPC = PPC / PER;              // lanes per chunk in chunk_totals
+    constexpr int LPC = ChunkLanes<NPART, PPC>::LPC;       // lanes per chunk in chunk_totals
+    constexpr int LUSED = ChunkLanes<NPART, PPC>::LUSED;   // lanes with distinct chunk totals
     constexpr int CPT = TILE / C;               // chunks per tile
     constexpr int SG = GradBytes<GK>::value;
     static_assert(TILE % C == 0, "a tile holds whole chunks");
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
     using SL = Stream<SG, ADAM>;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ uint64_t full[NSLOT];
-    __shared__ float red[2][NPART];
+    __shared__ __align__(16) float red[2][NPART];
     __shared__ uint32_t lmax[kMaxChunkLayers];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -373,10 +380,11 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
         const int64_t klast = (k0 + CPT - 1 < P.K - 1) ? k0 + CPT - 1 : P.K - 1;
         const int l0 = D.chunk_l0[k0];
         // this lane's chunk in chunk_totals, and its element count
-        const int64_t kq = k0 + lane / LPC;
+        const int lq = lane % LUSED;
+        const int64_t kq = k0 + lq / LPC;
         const int64_t nq_raw = P.N - kq * C;
         const float nq = (float)(nq_raw >= C ? C : (nq_raw > 0 ? nq_raw : 0));
-        const bool lane_stores_scale = (lane % LPC) == 0 && lane / LPC < CPT && kq < P.K;
+        const bool lane_stores_scale = lane < LUSED && (lq % LPC) == 0 && kq < P.K;
 
         int nv[SLOTS];
         int qsrc[SLOTS];       // lane holding the scale of this slot's chunk
