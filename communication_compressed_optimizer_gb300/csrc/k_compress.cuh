@@ -26,6 +26,7 @@
 // cover the 128 consecutive elements starting at s*NT*4 + w*128, which is one
 // leaf block of the canonical pairwise tree.
 #pragma once
+#include <atomic>
 #include <type_traits>
 
 #include "lamb1b_internal.cuh"
@@ -722,13 +723,17 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
     constexpr int TILE = NT * 4 * SLOTS;
     constexpr size_t smem = (size_t)NSLOT * Ring<TILE>::kSlot;
     auto kern = k_compress<NT, SLOTS, GK, NSLOT, C, ADAM, EB>;
-    // per-device launch shape, computed once per instantiation
-    static int cached_device = -1;
-    static int grid_cap = 0;
+    // Launch shape per device and instantiation, set up on first use.  A slot
+    // is published only after its device's function attributes are set, and
+    // concurrent first uses on one device just repeat the same settings, so
+    // host threads driving different GPUs need no lock.
+    constexpr int kCachedDevices = 64;
+    static std::atomic<int> grid_cap_of[kCachedDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (cached_device != dev) {
+    int grid_cap = dev < kCachedDevices ? grid_cap_of[dev].load(std::memory_order_acquire) : 0;
+    if (grid_cap == 0) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return e;
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -738,7 +743,7 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem))) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
         grid_cap = (per_sm > 0 ? per_sm : 1) * sms;
-        cached_device = dev;
+        if (dev < kCachedDevices) grid_cap_of[dev].store(grid_cap, std::memory_order_release);
     }
     const int64_t ntiles = P.Np / TILE;
     const unsigned grid = (unsigned)(ntiles < grid_cap ? ntiles : grid_cap);

@@ -106,6 +106,7 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
 }
 
 int grads_check(const lamb1b_ctx* ctx, const lamb1b_grads* g);
+bool is_device_ptr(const void* p, int device);
 
 // NVTX range around the host side of one stage (enqueue only), so profiler
 // timelines show which library call launched which kernels.
@@ -143,10 +144,15 @@ int grads_check(const lamb1b_ctx* ctx, const lamb1b_grads* g)
         const int64_t es = g->kind == LAMB1B_GRAD_F32 ? 4 : 2;
         if (!g->ptr || g->ld < ctx->P.N) return LAMB1B_ERR_ARG;
         if ((reinterpret_cast<uintptr_t>(g->ptr) & 15u) || ((g->ld * es) & 15)) return LAMB1B_ERR_ALIGN;
+        // the kernels stage gradients with bulk copies from this GPU's memory
+        if (!is_device_ptr(g->ptr, ctx->device)) return LAMB1B_ERR_ARG;
         return LAMB1B_OK;
     }
     case LAMB1B_GRAD_PHILOX:
         if (!g->layer_std || !finite(g->heavy_scale)) return LAMB1B_ERR_ARG;
+        if (!is_device_ptr(g->layer_std, ctx->device) ||
+            (g->layer_heavy && !is_device_ptr(g->layer_heavy, ctx->device)))
+            return LAMB1B_ERR_ARG;
         return LAMB1B_OK;
     default:
         return LAMB1B_ERR_ARG;

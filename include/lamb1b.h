@@ -113,7 +113,9 @@ typedef enum {
  *     is drawn from Philox4x32-10 keyed by `seed` (the synthetic-workload
  *     definition of include/lamb1b_gen.h): layer_std[l] * N(0,1) for tensor l,
  *     or heavy_scale * Student-t(3) where layer_heavy[l] != 0.  layer_std and
- *     layer_heavy are device arrays of L entries. */
+ *     layer_heavy are device arrays of L entries.
+ * A step returns LAMB1B_ERR_ARG, before any launch, when ptr (F32 / BF16) or
+ * layer_std / layer_heavy (PHILOX) is not memory of the context's GPU. */
 typedef struct {
     int32_t kind;
     int32_t pad0;

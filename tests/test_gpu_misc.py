@@ -249,6 +249,17 @@ def test_call_order_and_argument_errors():
     rc = L.lamb1b_init(ctypes.byref(ctx), arr, len(arr), ctypes.byref(h), ctypes.c_void_p(hp_ptr),
                        ctypes.c_void_p(ws.data_ptr()), ws.numel(), None)
     assert rc == _abi.ERR_ARG and ctx.value is None
+    # nor as gradients: rejected on the host before any launch
+    hg = np.zeros(wl.W * ld + 64, np.float32)
+    d = _abi.GradsDesc()
+    d.kind, d.ld = pkg.GRAD_F32, ld
+    d.ptr = (hg.ctypes.data + 255) // 256 * 256
+    assert L.lamb1b_compress_step(opt._ctx, ctypes.byref(d), None) == _abi.ERR_ARG
+    std_host = np.ones(wl.L + 16, np.float32)
+    d = _abi.GradsDesc()
+    d.kind, d.layer_std, d.heavy_scale = pkg.GRAD_PHILOX, (std_host.ctypes.data + 15) // 16 * 16, 1e-3
+    assert L.lamb1b_compress_step(opt._ctx, ctypes.byref(d), None) == _abi.ERR_ARG
+    assert opt.state()["t"] == 1
 
 
 def test_trace_events_time_every_kernel_of_a_step():
