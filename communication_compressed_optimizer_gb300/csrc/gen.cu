@@ -4,6 +4,7 @@
 #include "lamb1b_gen.h"
 #include "lamb1b.h"
 #include "philox.cuh"
+#include "device_ptr.h"
 
 namespace lamb1b {
 
@@ -64,6 +65,7 @@ extern "C" int lamb1b_gen_grads(void* out_dev, int64_t ld, int32_t W, int32_t bf
         N += layer_numel[l];
     }
     if (ld < N) return LAMB1B_ERR_ARG;
+    if (!lamb1b::is_current_device_ptr(out_dev)) return LAMB1B_ERR_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     for (int32_t l = 0; l < L; ++l) {
         const int64_t lo = layer_off[l], hi = lo + layer_numel[l];
@@ -86,6 +88,7 @@ extern "C" int lamb1b_gen_params(float* out_dev, int64_t lo, int64_t hi, float s
 {
     if (!out_dev || lo < 0 || hi < lo) return LAMB1B_ERR_ARG;
     if (hi == lo) return LAMB1B_OK;
+    if (!lamb1b::is_current_device_ptr(out_dev)) return LAMB1B_ERR_ARG;
     const int64_t nq = (hi - 1) / 4 - lo / 4 + 1;
     lamb1b::k_gen_params<<<(unsigned)((nq + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         out_dev, lo, hi, std, seed);

@@ -11,6 +11,7 @@
 
 #include "lamb1b.h"
 #include "lamb1b_internal.cuh"
+#include "device_ptr.h"
 
 using lamb1b::Dev;
 using lamb1b::Grads;
@@ -106,7 +107,7 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
 }
 
 int grads_check(const lamb1b_ctx* ctx, const lamb1b_grads* g);
-bool is_device_ptr(const void* p, int device);
+using lamb1b::is_device_ptr;
 
 // NVTX range around the host side of one stage (enqueue only), so profiler
 // timelines show which library call launched which kernels.
@@ -180,15 +181,6 @@ int device_check(const lamb1b_ctx* ctx)
     return dev == ctx->device ? LAMB1B_OK : LAMB1B_ERR_DEVICE;
 }
 
-bool is_device_ptr(const void* p, int device)
-{
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == device;
-}
 
 }  // namespace
 

@@ -10,6 +10,7 @@
 
 #include "lamb1b.h"
 #include "lamb1b_internal.cuh"
+#include "device_ptr.h"
 
 namespace lamb1b {
 namespace noalloc {
@@ -161,6 +162,8 @@ extern "C" int lamb1b_tensor_sumsq_noalloc(const float* x_dev, const lamb1b_laye
     if (!x_dev || !out_dev || !layers || L < 1) return LAMB1B_ERR_ARG;
     if (L > kMaxLayers) return LAMB1B_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(x_dev) & 15u) return LAMB1B_ERR_ALIGN;
+    if (!lamb1b::is_current_device_ptr(x_dev) || !lamb1b::is_current_device_ptr(out_dev))
+        return LAMB1B_ERR_ARG;
     std::vector<int64_t> tab(3 * (size_t)L + 1);
     int64_t* off = tab.data();
     int64_t* end = off + L;

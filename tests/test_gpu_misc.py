@@ -260,6 +260,13 @@ def test_call_order_and_argument_errors():
     d.kind, d.layer_std, d.heavy_scale = pkg.GRAD_PHILOX, (std_host.ctypes.data + 15) // 16 * 16, 1e-3
     assert L.lamb1b_compress_step(opt._ctx, ctypes.byref(d), None) == _abi.ERR_ARG
     assert opt.state()["t"] == 1
+    # the generator and the allocation-free sums check their device pointers too
+    assert L.lamb1b_gen_params(ctypes.c_void_p(hp_ptr), 0, 64, 1.0, 0, None) == _abi.ERR_ARG
+    out = torch.zeros(len(arr), device="cuda")
+    assert L.lamb1b_tensor_sumsq_noalloc(ctypes.c_void_p(hp_ptr), arr, len(arr),
+                                         ctypes.c_void_p(out.data_ptr()), None) == _abi.ERR_ARG
+    assert L.lamb1b_tensor_sumsq_noalloc(ctypes.c_void_p(x.data_ptr()), arr, len(arr),
+                                         ctypes.c_void_p(hp_ptr), None) == _abi.ERR_ARG
 
 
 def test_trace_events_time_every_kernel_of_a_step():
