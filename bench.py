@@ -636,11 +636,13 @@ def run_e2e(args, opt, wl, g, regen, t, ld):
 
 def main():
     args = parse_args()
-    world, rank, local = dist_setup(args)
     if args.impl == "reference":
-        run_reference(args, world, rank)
-    else:
-        run_ours(args, world, rank, local)
+        # the CPU oracle needs no collective: rank 0 alone runs it, the others
+        # exit without joining a process group
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
