@@ -123,7 +123,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha1()
-    for f in ("k_compress.cuh", "k_compress.cu", "lamb1b_internal.cuh"):
+    for f in ("k_compress.cuh", "k_compress.cu", "lamb1b_internal.cuh", "philox.cuh"):
         with open(os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
