@@ -533,6 +533,9 @@ def run_ours(args, world, rank, local):
                  "frac_of_peak": step_bytes(wl, args.variant, args.errors) / (ms_per_step / 1e3) / 1e9 / peak,
                  "kernel_ms": {"compress": k_avg, "factor": statistics.mean(factor_ms),
                                "update": statistics.mean(upd_ms)},
+                 # the step's other streaming kernel, against the same peak
+                 "update_gbs": update_kernel_bytes(wl) / (statistics.mean(upd_ms) / 1e3) / 1e9,
+                 "update_frac_of_peak": update_kernel_bytes(wl) / (statistics.mean(upd_ms) / 1e3) / 1e9 / peak,
                  "ms_p10": float(np.percentile(step_ms, 10)),
                  "ms_p50": float(np.percentile(step_ms, 50)),
                  "ms_p90": float(np.percentile(step_ms, 90)),
