@@ -1,0 +1,124 @@
+"""Index arithmetic of the fused compression kernel, checked on the CPU for
+every launch shape its dispatch table uses (parsed from the kernel header, so
+a new shape is checked as soon as it is added).  Each check restates one
+bound the kernel relies on: shared-memory ring and partial-sum buffers, the
+lanes that hold chunk totals, the sign-word and error stores of a tile, and
+the 16-byte sizes of the bulk copies."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HDR = os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", "k_compress.cuh")
+SMEM_PER_BLOCK = 227 * 1024          # opt-in shared memory per CTA on sm_103a
+SMEM_PER_SM = 228 * 1024
+
+
+def dispatched_shapes():
+    text = open(HDR).read()
+    body = text[text.index("cudaError_t launch_fused_all_chunks"):]
+    shapes = set()
+    for m in re.finditer(r"launch_grad<(\d+), (\d+), (\d+), (\d+), ADAM, EB>", body):
+        nt, slots, nslot, c = map(int, m.groups())
+        for gk in (0, 1, 2):
+            shapes.add((nt, slots, nslot, c, gk))
+    for m in re.finditer(r"launch_one<(\d+), (\d+), kGrad(F32|BF16|Philox), (\d+), (\d+), ADAM, EB>", body):
+        nt, slots, kind, nslot, c = m.groups()
+        shapes.add((int(nt), int(slots), int(nslot), int(c), {"F32": 0, "BF16": 1, "Philox": 2}[kind]))
+    return sorted(shapes)
+
+
+SHAPES = dispatched_shapes()
+
+
+def test_dispatch_table_was_parsed():
+    cs = {s[3] for s in SHAPES}
+    assert cs == {256, 512, 1024, 2048, 4096, 8192}
+    assert (512, 2, 7, 4096, 0) in SHAPES
+
+
+@pytest.mark.parametrize("nt,slots,nslot,c,gk", SHAPES)
+def test_shape_bounds(nt, slots, nslot, c, gk):
+    tile = nt * 4 * slots
+    nwarp = nt // 32
+    npart = tile // 128
+    ppc = c // 128
+    cpt = tile // c
+    assert nt % 32 == 0 and nt <= 1024
+    assert tile % c == 0 and cpt >= 1, "a tile holds whole chunks"
+    assert slots & (slots - 1) == 0 and slots <= 8, "pack_words handles up to 8 slots"
+    # ring: NSLOT slots of TILE floats; two CTAs per SM when two rings fit
+    slot_bytes = tile * 4
+    min_blocks = 2 if nslot * slot_bytes <= 112 * 1024 else 1
+    static = 2 * npart * 4 + 64 * 4 + nslot * 8            # red, lmax, mbarriers
+    assert nslot * slot_bytes + static <= SMEM_PER_BLOCK
+    assert min_blocks * (nslot * slot_bytes + static + 1024) <= SMEM_PER_SM
+    assert 65536 // (nt * min_blocks) >= 64, "the launch bound leaves at least 64 registers"
+    # the 128-leaf partial of slot s, warp w is red[s * NWARP + w], in element order
+    for s in range(slots):
+        for w in range(nwarp):
+            idx = s * nwarp + w
+            assert idx < npart and idx * 128 == s * nt * 4 + w * 128
+    # chunk totals: G partials per lane (one vector load), LPC lanes per chunk
+    g = 4 if ppc >= 4 else ppc
+    lpc = ppc // g
+    lused = npart // g
+    assert ppc % g == 0 and lused * g == npart and 1 <= lused <= 32
+    assert (npart * 4) % 16 == 0, "red[1] stays 16-byte aligned for the vector loads"
+    for lane in range(32):
+        lq = lane % lused
+        assert lq * g + g <= npart
+        assert lq // lpc < cpt                                   # a chunk of this tile
+    # the lane holding a slot's chunk scale (qsrc) is one with that chunk's total
+    for s in range(slots):
+        for w in range(nwarp):
+            chunk = (s * nt * 4 + w * 128) // c
+            src = chunk * lpc
+            assert src < lused and (src % lused) // lpc == chunk
+    # sign words: lanes with (lane & 7) < SLOTS store word (lane >> 3) of slot
+    # tree_block(lane), all inside the tile's TILE/32 words
+    def tree_block(lane):
+        b, o, n = 0, 1, slots
+        while n > 1:
+            if lane & o:
+                b += n // 2
+            n //= 2
+            o <<= 1
+        return b
+    words = set()
+    for w in range(nwarp):
+        for lane in range(32):
+            if (lane & 7) < slots:
+                wd = (w * 128) // 32 + (lane >> 3) + tree_block(lane) * (nt * 4 // 32)
+                assert 0 <= wd < tile // 32
+                words.add(wd)
+    assert len(words) == tile // 32, "every word of the tile is stored exactly once per warp set"
+    # error stores: thread tid writes 4 elements at s*NT*4 + tid*4 inside the tile
+    assert (slots - 1) * nt * 4 + (nt - 1) * 4 + 4 <= tile
+    # bulk copies: slot-sized copies and the packed-momentum words are 16-byte multiples
+    assert slot_bytes % 16 == 0 and (tile // 8) % 16 == 0
+    grad_bytes = {0: 4, 1: 2, 2: 0}[gk]
+    if grad_bytes:
+        assert (tile * grad_bytes) % 16 == 0
+        # a partial last tile copies (N - base) gradients rounded up to 16 bytes: inside a row of
+        # the smallest leading dimension the API accepts (ld >= N, ld * bytes a multiple of 16)
+        per16 = 16 // grad_bytes
+        for n in range(1, 2 * tile + 40):
+            ld = -(-n // per16) * per16
+            base = (n - 1) // tile * tile
+            copied = -(-(n - base) * grad_bytes // 16) * 16
+            assert base * grad_bytes + copied <= ld * grad_bytes, n
+    # scale span of the packed momentum: from k0 & ~3, (k0 & 3) + CPT floats rounded up to 16
+    # bytes, for every tile of the padded length, never past scale_s[K + 16) (the region has 16
+    # floats of padding), and it fits in the momentum slot after the tile's sign words
+    step = max(c, 4096)
+    for n in list(range(1, 3 * step + 2, 97)) + [step * k + d for k in (1, 2, 5) for d in (-1, 0, 1)]:
+        k = -(-n // c)
+        npad = -(-n // step) * step
+        for t in range(npad // tile):
+            k0 = t * tile // c
+            ka = k0 & ~3
+            sbytes = ((k0 - ka + cpt) * 4 + 15) // 16 * 16
+            assert ka + sbytes // 4 <= k + 16, (n, t)
+            assert tile // 8 + sbytes <= slot_bytes
