@@ -71,6 +71,15 @@ MUTATIONS = [
      "update_tensor(s, l, 1.0f);", "update_tensor(s, l, s->c_bar[l]);"),
     ("bfloat16 storage truncates instead of rounding to nearest even",
      "((b + 0x7FFFu + ((b >> 16) & 1u)) >> 16)", "(b >> 16)"),
+    ("1-bit Adam warmup applies LAMB's trust ratio",
+     "        if (s->variant == 1) {\n            /* 1-bit Adam's warmup is vanilla Adam",
+     "        if (s->variant == 99) {\n            /* 1-bit Adam's warmup is vanilla Adam"),
+    ("server error kept unrounded under bfloat16 storage",
+     "for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = store_err(s, err[j]);",
+     "for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = err[j];"),
+    ("1-bit Adam tracks a fresh variance",
+     "        if (s->variant == 1) {      /* 1-bit Adam: no fresh variance, no ratio */",
+     "        if (s->variant == 99) {      /* 1-bit Adam: no fresh variance, no ratio */"),
 ]
 
 

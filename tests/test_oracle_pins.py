@@ -606,7 +606,7 @@ def test_bf16_storage_rounding_matches_torch():
 def test_bf16_error_storage_rounds_the_fp32_error_once():
     """From zero errors, one compression step of the bf16-storage variant
     sends the same words and scales as the fp32 variant and keeps the
-    fp32 variant's new errors rounded to bfloat16."""
+    fp32 variant's new worker and server errors rounded to bfloat16."""
     rng = np.random.default_rng(14)
     states = []
     for eb in (0, 1):
@@ -623,6 +623,11 @@ def test_bf16_error_storage_rounds_the_fp32_error_once():
     np.testing.assert_array_equal(a.scale_w, b.scale_w)
     want = np.array([oracle.bf16_round(v) for v in a.e_w.ravel()], np.float32).reshape(a.e_w.shape)
     np.testing.assert_array_equal(b.e_w.view(np.uint32), want.view(np.uint32))
+    # the server sees the same average (same words and scales), so its kept error is the
+    # binary32 one rounded once as well
+    np.testing.assert_array_equal(a.signs_s, b.signs_s)
+    want_s = np.array([oracle.bf16_round(v) for v in a.e_s], np.float32)
+    np.testing.assert_array_equal(b.e_s.view(np.uint32), want_s.view(np.uint32))
 
 
 def test_bf16_error_feedback_telescopes_within_storage_rounding():
