@@ -77,6 +77,8 @@ MUTATIONS = [
     ("server error kept unrounded under bfloat16 storage",
      "for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = store_err(s, err[j]);",
      "for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = err[j];"),
+    ("a NaN ratio ignored by the per-tensor maximum",
+     "if (rho) rho[j] = (r != r) ? INFINITY : r;", "if (rho) rho[j] = r;"),
     ("1-bit Adam tracks a fresh variance",
      "        if (s->variant == 1) {      /* 1-bit Adam: no fresh variance, no ratio */",
      "        if (s->variant == 99) {      /* 1-bit Adam: no fresh variance, no ratio */"),

@@ -479,6 +479,23 @@ def test_soft_threshold_growth_closed_form():
         np.testing.assert_allclose(o2.r_prev, max(0.5, 0.9 ** t), rtol=2e-6)
 
 
+def test_nan_ratio_counts_as_infinity():
+    """A NaN gradient makes the element's ratio NaN; the per-tensor maximum
+    counts it as +Inf (reading R19), so the factor rises by the soft
+    threshold only (clip(Inf, fmin, fmax) = fmax, then at most 1.1 r_prev),
+    and the other tensor is unaffected."""
+    rng = np.random.default_rng(26)
+    o = _fresh([1024, 1024], 2, 256, HP, x0=(rng.standard_normal(2048) * 2e-2).astype(np.float32))
+    o.v[:] = 1e-4
+    o.freeze()
+    g = (rng.standard_normal((2, 2048)) * 1e-2).astype(np.float32)
+    g[1, 100] = np.nan
+    o.compress_step(g)
+    assert o.R[0] == np.inf
+    assert o.r_prev[0] == np.float32(np.float32(1.1) * np.float32(1.0))
+    assert np.isfinite(o.R[1]) and np.isfinite(o.r_prev[1])
+
+
 def test_layer_factor_clip_definition():
     """clip(x, a, b) = min{max{x, a}, b} (LAMB background, footnote 4),
     applied twice: the hard bounds, then +-threshold around r_prev."""
