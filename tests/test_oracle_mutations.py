@@ -77,6 +77,10 @@ MUTATIONS = [
     ("server error kept unrounded under bfloat16 storage",
      "for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = store_err(s, err[j]);",
      "for (int64_t j = 0; j < n; ++j) s->e_s[base + j] = err[j];"),
+    ("sign words not cleared before packing",
+     "for (int32_t q = 0; q < C / 32; ++q) words[q] = 0u;", ""),
+    ("no weight decay in the warmup direction",
+     "u[i] = fadd(fdiv(s->m[i], d), fmul(s->wd, s->x[i]));", "u[i] = fdiv(s->m[i], d);"),
     ("a NaN ratio ignored by the per-tensor maximum",
      "if (rho) rho[j] = (r != r) ? INFINITY : r;", "if (rho) rho[j] = r;"),
     ("1-bit Adam tracks a fresh variance",
