@@ -163,9 +163,10 @@ class OneBitLamb:
 
     def set_fault_injection(self, skip_copy=-1, wait_tries=0):
         """Testing hook: the first CTA of later compression steps leaves out
-        bulk copy number skip_copy (-1: none); every copy wait gives up after
-        wait_tries try_wait calls (0: the default).  A step that gave up is
-        reported by check_status() as a timeout."""
+        bulk copy number skip_copy (-1: none); that CTA's copy waits give up
+        after wait_tries try_wait calls (0: the default; other CTAs always
+        keep the default).  A step that gave up is reported by check_status()
+        as a timeout."""
         _abi.check("lamb1b_set_fault_injection",
                    self._lib.lamb1b_set_fault_injection(self._ctx, int(skip_copy), int(wait_tries)))
 

@@ -3,18 +3,22 @@
  *
  * Method: "1-bit LAMB: Communication Efficient Large-Scale Large-Batch
  * Training with LAMB's Convergence Speed" (Li, Awan, Tang, Rajbhandari, He;
- * arXiv 2104.06069).  Two stages over a flat binary32 parameter buffer cut
- * into per-tensor "layers":
+ * arXiv 2104.06069).  Citations below name a section of that paper's HTML
+ * text ("1-bit LAMB, <section>"); its headings were lost in extraction, so
+ * sections are named by their content.  Two stages over a flat binary32
+ * parameter buffer cut into per-tensor "layers":
  *   - warmup: LAMB (Adam moments plus one clipped trust ratio per tensor;
- *     paper background on LAMB, footnote 4 for the clip);
+ *     1-bit LAMB, background section on LAMB, with its footnote 4 for the
+ *     clip definition);
  *   - compression: for W data-parallel workers held side by side in device
  *     memory, error-compensated 1-bit compression of each worker's momentum
- *     (one scale per chunk plus sign bits packed 32 per word; background on
- *     error-compensated compression), the compressed allreduce's gather,
- *     average and scatter phases (section 5 summary) with server-side error
- *     feedback, and the frozen-variance update with the layerwise factor
- *     computed from the reconstructed gradient under soft thresholds (section
- *     4 summary).
+ *     (one scale per chunk plus sign bits packed 32 per word; 1-bit LAMB,
+ *     background section on error-compensated compression), the compressed
+ *     allreduce's gather, average and scatter phases (1-bit LAMB, section 5,
+ *     the NCCL-based backend) with server-side error feedback, and the
+ *     frozen-variance update with the layerwise factor computed from the
+ *     reconstructed gradient under soft thresholds (1-bit LAMB, section 4
+ *     summary of the algorithm).
  *
  * Conventions shared by every entry point:
  *   - Pointers named *_dev are device pointers on the device that was current
@@ -60,8 +64,8 @@ enum {
                                    results are not valid                        */
 };
 
-/* One tensor of the model ("each tensor has its own scaling coefficient",
- * paper background on LAMB).  Tensors are contiguous and ascending:
+/* One tensor of the model (1-bit LAMB, background section on LAMB: every
+ * tensor, weight or bias, has its own scaling coefficient).  Tensors are contiguous and ascending:
  * layer[0].offset == 0, layer[l+1].offset == layer[l].offset + layer[l].numel,
  * numel >= 1; N = sum of numel. */
 typedef struct {
@@ -191,8 +195,9 @@ int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t L,
                 const lamb1b_hparams* hp, float* params_dev,
                 void* workspace_dev, size_t workspace_bytes, void* stream);
 
-/* Warmup stage, one LAMB step (paper background on LAMB; the uncompressed
- * warmup of 1-bit LAMB, introduction):
+/* Warmup stage, one LAMB step (1-bit LAMB, background section on LAMB: the
+ * symbol list and clip definition of its update rule; the introduction: LAMB
+ * runs uncompressed as the warmup stage):
  *   gbar = (sum_w g_w) / W, summed in ascending w
  *   m = beta1 m + (1-beta1) gbar;  v = beta2 v + (1-beta2) gbar^2
  *   u = m / (sqrt(v) + eps) + weight_decay x
@@ -202,13 +207,19 @@ int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t L,
  * Errors: STATE after lamb1b_freeze_variance; ARG/ALIGN for bad gradients. */
 int lamb1b_warmup_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, void* stream);
 
-/* Stage switch (1-bit Adam's variance freeze, paper background): v is kept as
+/* Stage switch (1-bit LAMB, background section on 1-bit Adam, and the
+ * 1-bit Adam abstract: the variance is frozen after the warmup): v is kept as
  * the fixed preconditioner, v_fresh = v, worker and server errors = 0,
  * r_prev = 1; c_bar is fixed from here on.  Allowed once, before any
  * compression step.  Errors: STATE. */
 int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream);
 
-/* Compression stage, one step.  Per chunk k and worker w (gather phase):
+/* Compression stage, one step (1-bit LAMB: the introduction's compression
+ * stage, momentum SGD preconditioned by the frozen variance; the background
+ * section on error-compensated compression for the worker and server
+ * compressors; section 5 for the gather, average and scatter phases; the
+ * section 4 summary for the reconstructed gradient and the soft thresholds).
+ * Per chunk k and worker w (gather phase):
  *   z = (beta1 m + (1-beta1) g_w) + e_w
  *   s_wk = sqrt(sum_chunk z^2 / n_k);  bit = !(z < 0);  e_w = z -+ s_wk
  * server (average and scatter phases):
@@ -263,9 +274,11 @@ int lamb1b_sync_momentum(lamb1b_ctx* ctx, void* stream);
  * skip_copy >= 0 makes the first CTA of every later compression step leave
  * out the copy at that position of its copy sequence (0 = the first tile's
  * momentum, then per worker its gradient and error, ...), so the wait for it
- * can only run out; skip_copy = -1 turns this off.  wait_tries bounds every
- * wait, in mbarrier.try_wait calls; 0 restores the default (2^24, seconds).
- * A step whose wait ran out stops early, records LAMB1B_ERR_TIMEOUT for
+ * can only run out; skip_copy = -1 turns this off.  wait_tries bounds the
+ * copy waits of that first CTA, in mbarrier.try_wait calls; 0 restores the
+ * default (2^24, seconds).  Every other CTA's waits, and the wait with which a
+ * CTA that gave up lets its issued copies land before it exits, keep the
+ * default bound.  A step whose wait ran out stops early, records LAMB1B_ERR_TIMEOUT for
  * lamb1b_check_status and leaves the optimizer state undefined (restore it
  * from a checkpoint); the CUDA context stays usable.  No GPU fault is raised.
  * Errors: ARG for a NULL ctx or skip_copy < -1. */

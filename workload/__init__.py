@@ -261,13 +261,20 @@ def gen_grads(wl: Workload, t: int, w: int, N: int | None = None,
     return out
 
 
-def gen_grads_range(wl: Workload, t: int, w: int, lo: int, hi: int) -> np.ndarray:
+def grad_tables(wl: Workload):
+    """The per-tensor arrays the gradient generator reads (offsets, sizes,
+    std, Student-t flags), for callers that generate many ranges of one
+    workload."""
+    return (wl.offsets, wl.numels, wl.layer_std, wl.layer_heavy)
+
+
+def gen_grads_range(wl: Workload, t: int, w: int, lo: int, hi: int, tables=None) -> np.ndarray:
     """Binary32 gradients of worker w at step t for elements [lo, hi) (the
-    bf16 workload's values before rounding to bf16)."""
+    bf16 workload's values before rounding to bf16).  tables: the workload's
+    grad_tables(), if the caller keeps them."""
     out = np.empty(hi - lo, dtype=np.float32)
-    off, num = wl.offsets, wl.numels
-    std, heavy = wl.layer_std, wl.layer_heavy
-    lib().wl_gen_grads_range_f32(wl.seed, t, w, lo, hi, wl.L, _ptr(off), _ptr(num), _ptr(std),
+    off, num, std, heavy = grad_tables(wl) if tables is None else tables
+    lib().wl_gen_grads_range_f32(wl.seed, t, w, lo, hi, len(off), _ptr(off), _ptr(num), _ptr(std),
                                  _ptr(heavy), wl.heavy_scale, _ptr(out))
     return out
 

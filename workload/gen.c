@@ -157,17 +157,29 @@ uint16_t wl_bf16_rne(float f)
 
 /* ---- streams ------------------------------------------------------------ */
 
+/* The four normals of one Philox call of a normal stream, kept while a loop
+ * walks the four elements that share the call (q = i / 4).  Only a cache:
+ * every value is the one a fresh call would give. */
+typedef struct {
+    uint64_t q;
+    int valid;
+    float z[4];
+} normal_cache;
+
 /* One gradient value for element i of worker w at step t.  `layer` is the
  * tensor holding i; std/heavy describe it. */
 static float grad_value(uint64_t seed, int64_t i, uint32_t t, uint32_t w,
-                        float std, int heavy, float heavy_scale)
+                        float std, int heavy, float heavy_scale, normal_cache* nc)
 {
     if (heavy)
         return heavy_scale * wl_student_t3(seed, i, t, w);
     uint64_t q = (uint64_t)i >> 2;
-    float z[4];
-    wl_normal4(seed, (uint32_t)q, (uint32_t)(q >> 32), t, w, z);
-    return std * z[i & 3];
+    if (!nc->valid || nc->q != q) {
+        wl_normal4(seed, (uint32_t)q, (uint32_t)(q >> 32), t, w, nc->z);
+        nc->q = q;
+        nc->valid = 1;
+    }
+    return std * nc->z[i & 3];
 }
 
 /* Gradients of worker w at step t for elements [0, N), written to out[0..N).
@@ -181,8 +193,9 @@ void wl_gen_grads_f32(uint64_t seed, int64_t t, int32_t w, int64_t N, int32_t L,
         int64_t lo = off[l], hi = off[l] + numel[l];
         if (hi > N) hi = N;
         int hv = heavy ? heavy[l] != 0 : 0;
+        normal_cache nc = {0, 0, {0.0f, 0.0f, 0.0f, 0.0f}};
         for (int64_t i = lo; i < hi; ++i)
-            out[i] = grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale);
+            out[i] = grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale, &nc);
     }
 }
 
@@ -195,18 +208,26 @@ void wl_gen_grads_bf16(uint64_t seed, int64_t t, int32_t w, int64_t N, int32_t L
         int64_t lo = off[l], hi = off[l] + numel[l];
         if (hi > N) hi = N;
         int hv = heavy ? heavy[l] != 0 : 0;
+        normal_cache nc = {0, 0, {0.0f, 0.0f, 0.0f, 0.0f}};
         for (int64_t i = lo; i < hi; ++i)
-            out[i] = wl_bf16_rne(grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale));
+            out[i] = wl_bf16_rne(grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale,
+                                            &nc));
     }
 }
 
 /* Initial parameters: std * Z, stream 0x7FFFFFFF, t = 0, elements [lo, hi). */
 void wl_gen_params(uint64_t seed, int64_t lo, int64_t hi, float std, float* out)
 {
+    uint64_t qz = 0;
+    int have = 0;
+    float z[4];
     for (int64_t i = lo; i < hi; ++i) {
         uint64_t q = (uint64_t)i >> 2;
-        float z[4];
-        wl_normal4(seed, (uint32_t)q, (uint32_t)(q >> 32), 0u, 0x7FFFFFFFu, z);
+        if (!have || q != qz) {
+            wl_normal4(seed, (uint32_t)q, (uint32_t)(q >> 32), 0u, 0x7FFFFFFFu, z);
+            qz = q;
+            have = 1;
+        }
         out[i - lo] = std * z[i & 3];
     }
 }
@@ -219,9 +240,10 @@ void wl_gen_grads_range_f32(uint64_t seed, int64_t t, int32_t w, int64_t lo, int
                             float* out)
 {
     int32_t l = 0;
+    normal_cache nc = {0, 0, {0.0f, 0.0f, 0.0f, 0.0f}};
     for (int64_t i = lo; i < hi; ++i) {
         while (l < L - 1 && i >= off[l] + numel[l]) ++l;
         int hv = heavy ? heavy[l] != 0 : 0;
-        out[i - lo] = grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale);
+        out[i - lo] = grad_value(seed, i, (uint32_t)t, (uint32_t)w, std[l], hv, heavy_scale, &nc);
     }
 }
