@@ -51,6 +51,8 @@ def parse_args():
                    help="override the workload's chunk size C (the named workloads fix it)")
     p.add_argument("--workers", type=int, default=0,
                    help="override the workload's worker count W (the named workloads fix it)")
+    p.add_argument("--first-tensor", type=int, default=0,
+                   help="drop the tensors before this index of the table (profiling)")
     p.add_argument("--max-params", type=int, default=0,
                    help="keep only the leading tensors up to this many parameters (profiling)")
     p.add_argument("--warmup-stage-steps", type=int, default=-1,
@@ -70,6 +72,9 @@ def get_workload(args):
     if args.workers:
         wl.W = args.workers
         wl.name = f"{wl.name}[W={args.workers}]"
+    if args.first_tensor:
+        wl.tensors = wl.tensors[args.first_tensor:]
+        wl.name = f"{wl.name}[{args.first_tensor}:]"
     if args.max_params:
         keep, n = [], 0
         for name, shape in wl.tensors:

@@ -215,6 +215,63 @@ __device__ __forceinline__ void issue_item(int64_t t, int r, RingPos<NSLOT> p, i
     }
 }
 
+// Plain arrival on an mbarrier (release: this thread's earlier shared-memory
+// reads and writes are ordered before it).
+__device__ __forceinline__ void bar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tma::saddr(bar)) : "memory");
+}
+
+// One arrival per warp: the warp's lanes synchronise (which orders their
+// earlier shared-memory accesses before lane 0's), then lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) bar_arrive(bar);
+}
+
+// Wait for phase `parity` of a barrier that other warps of this CTA complete
+// (the gradient handoff): bounded like the copy waits (kDefaultWaitTries
+// try_wait calls, seconds), and left early once *stop is set (checked every
+// 256 tries).  Returns whether the phase completed.
+__device__ __forceinline__ bool wait_handoff(uint64_t* bar, uint32_t parity, volatile int* stop)
+{
+    for (uint32_t it = 0; it < kDefaultWaitTries; ++it) {
+        if (tma::try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u && stop && *stop) return false;
+    }
+    return false;
+}
+
+// CTA barriers of the compressing threads.  With draw warps (DRAW) those are
+// the first NT threads only, synchronised on named barrier 1; otherwise the
+// whole CTA on barrier 0.
+template <int NT, bool DRAW>
+__device__ __forceinline__ bool sync_or(bool pred)
+{
+    if constexpr (!DRAW) {
+        return __syncthreads_or(pred) != 0;
+    } else {
+        uint32_t r;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.or.pred q, 1, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(r)
+            : "r"((uint32_t)pred), "n"(NT)
+            : "memory");
+        return r != 0;
+    }
+}
+
+template <int NT, bool DRAW>
+__device__ __forceinline__ void sync_all()
+{
+    if constexpr (!DRAW) __syncthreads();
+    else asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
 // Consumer side: wait for n consecutive slots starting at p.
 template <int NSLOT>
 __device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int n, uint32_t tries)
@@ -311,14 +368,122 @@ __device__ __forceinline__ void store_err4(void* base, int64_t off, const float 
     }
 }
 
-// Two CTAs per SM when two rings fit in shared memory, else one.
-template <int NT, int SLOTS, int NSLOT>
+// Two CTAs per SM when two rings fit in shared memory, else one; a CTA with
+// draw warps (NDRAW > 0) runs alone on its SM.
+template <int NT, int SLOTS, int NSLOT, int NDRAW = 0>
 struct MinBlocks {
-    static constexpr int value = (NSLOT * (NT * 4 * SLOTS) * 4 <= 112 * 1024) ? 2 : 1;
+    static constexpr int value =
+        NDRAW > 0 ? 1 : ((NSLOT * (NT * 4 * SLOTS) * 4 <= 112 * 1024) ? 2 : 1);
 };
 
-template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM, bool EB>
-__global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
+// Gradient tiles in flight between the draw warps and the compressing warps.
+constexpr int kDrawSlots = 3;
+
+// In-kernel gradients drawn by NDRAW dedicated threads (threads NT ..
+// NT+NDRAW-1 of the CTA): for every tile of the CTA and every worker, in the
+// order the compressing threads consume them, the tile's TILE gradient
+// values (layer_std[l] x N(0,1), or heavy_scale x Student-t(3) in flagged
+// tensors; 0 past N) are written into one of kDrawSlots shared-memory slots.
+// Slot k is handed over through mbarriers: gfull[k] completes when every
+// draw warp has written its part, gempty[k] when every compressing warp has
+// read its part (one arrival per warp).  Thread d draws the aligned groups of four at tile offsets
+// g*NDRAW*4 + d*4, so one warp writes 512 contiguous bytes per group.  The
+// draws are those of the stored-gradient definition (include/lamb1b_gen.h),
+// so the values are the same bits wherever they are computed.
+template <int TILE, int NDRAW>
+__device__ __forceinline__ void draw_gradients(const Problem& P, const Dev& D, const Grads& G,
+                                               float* gring, uint64_t* gfull, uint64_t* gempty,
+                                               int64_t nloc, volatile int* stop)
+{
+    constexpr int PG = TILE / (4 * NDRAW);          // groups of four per thread
+    static_assert(PG >= 1 && TILE % (4 * NDRAW) == 0, "draw split");
+    const int d = threadIdx.x - (int)(blockDim.x - NDRAW);
+    RingPos<kDrawSlots> gp;
+    for (int64_t ti = 0; ti < nloc; ++ti) {
+        const int64_t base = (blockIdx.x + ti * gridDim.x) * (int64_t)TILE;
+        float stdv[PG][4];
+        uint32_t heavy[PG];
+        int nvd[PG];
+        {
+            int l = D.chunk_l0[base >> P.log2c];
+            int64_t lend = D.layer_end[l];
+#pragma unroll
+            for (int g = 0; g < PG; ++g) {
+                const int64_t e = base + g * NDRAW * 4 + d * 4;
+                const int64_t r = P.N - e;
+                nvd[g] = r >= 4 ? 4 : (r > 0 ? (int)r : 0);
+                heavy[g] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    stdv[g][c] = 0.0f;
+                    if (c < nvd[g]) {
+                        while (e + c >= lend) { ++l; lend = D.layer_end[l]; }
+                        stdv[g][c] = G.layer_std[l];
+                        if (G.layer_heavy && G.layer_heavy[l]) heavy[g] |= 1u << c;
+                    }
+                }
+            }
+        }
+        bool all_normal = true, all_heavy = true;
+#pragma unroll
+        for (int g = 0; g < PG; ++g) {
+            all_normal = all_normal && heavy[g] == 0u;
+            all_heavy = all_heavy && heavy[g] == 0xFu;
+        }
+        for (int w = 0; w < P.W; ++w) {
+            // wait until the compressing threads have read this slot's last
+            // tile (a fresh slot passes at once); leave if they stopped
+            if (!wait_handoff(&gempty[gp.slot], gp.phase ^ 1u, stop)) {
+                if (!*stop) atomicOr(D.flags, 2u);
+                return;
+            }
+            float* slot = gring + gp.slot * TILE;
+            // each group of four is stored as soon as it is drawn (past N:
+            // zeros; the compressing threads mask those elements)
+            auto put = [&](int g, const float (&v)[4]) {
+                const float4 q = nvd[g] == 4 ? make_float4(v[0], v[1], v[2], v[3])
+                                             : make_float4(nvd[g] > 0 ? v[0] : 0.0f, nvd[g] > 1 ? v[1] : 0.0f,
+                                                           nvd[g] > 2 ? v[2] : 0.0f, 0.0f);
+                *reinterpret_cast<float4*>(slot + g * NDRAW * 4 + d * 4) = q;
+            };
+            if (all_heavy) {
+                // four independent Student-t chains at a time
+#pragma unroll 1
+                for (int g = 0; g < PG; ++g) {
+                    float v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        v[c] = fmul(G.heavy_scale,
+                                    gen::student_t3(G.seed, base + g * NDRAW * 4 + d * 4 + c, G.t, (uint32_t)w));
+                    put(g, v);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < PG; ++g) {
+                    float v[4];
+                    gen::grads_normal4(G.seed, (uint64_t)(base + g * NDRAW * 4 + d * 4) >> 2, G.t,
+                                       (uint32_t)w, v);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) v[c] = fmul(stdv[g][c], v[c]);
+                    if (!all_normal && heavy[g]) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if ((heavy[g] >> c) & 1u)
+                                v[c] = fmul(G.heavy_scale,
+                                            gen::student_t3(G.seed, base + g * NDRAW * 4 + d * 4 + c, G.t,
+                                                            (uint32_t)w));
+                    }
+                    put(g, v);
+                }
+            }
+            warp_arrive(&gfull[gp.slot]);
+            gp = gp.plus(1);
+        }
+    }
+}
+
+template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM, bool EB, int NDRAW = 0>
+__global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value))
     k_compress(const Problem P, const Dev D, const Grads G)
 {
     constexpr int NWARP = NT / 32;
@@ -329,13 +494,21 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
     constexpr int LUSED = ChunkLanes<NPART, PPC>::LUSED;   // lanes with distinct chunk totals
     constexpr int CPT = TILE / C;               // chunks per tile
     constexpr int SG = GradBytes<GK>::value;
+    // in-kernel gradients drawn by dedicated warps (see draw_gradients)
+    constexpr bool DRAW = GK == kGradPhilox && NDRAW > 0;
+    constexpr int GKC = DRAW ? kGradF32 : GK;   // how the compressing threads read gradients
+    static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;
     using SL = Stream<SG, ADAM>;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ uint64_t full[NSLOT];
+    __shared__ uint64_t gfull[DRAW ? kDrawSlots : 1], gempty[DRAW ? kDrawSlots : 1];
+    __shared__ int stop_draw;
     __shared__ __align__(16) float red[2][NPART];
     __shared__ uint32_t lmax[kMaxChunkLayers];
+    // gradient slots of the draw warps follow the copy ring
+    float* const gring = reinterpret_cast<float*>(ring + (size_t)NSLOT * R::kSlot);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int W = P.W;
@@ -350,10 +523,24 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
 
     if (tid == 0) {
         for (int s = 0; s < NSLOT; ++s) tma::bar_init(&full[s], 1);
+        if constexpr (DRAW) {
+            for (int s = 0; s < kDrawSlots; ++s) {
+                tma::bar_init(&gfull[s], NDRAW / 32);     // one arrival per warp
+                tma::bar_init(&gempty[s], NT / 32);
+            }
+            stop_draw = 0;
+        }
         tma::fence_init();
     }
     for (int i = tid; i < kMaxChunkLayers; i += NT) lmax[i] = 0u;
     __syncthreads();
+    if constexpr (DRAW) {
+        if (tid >= NT) {
+            draw_gradients<TILE, NDRAW>(P, D, G, gring, gfull, gempty, nloc, &stop_draw);
+            return;
+        }
+    }
+    RingPos<kDrawSlots> gcp;                  // next gradient slot to read (DRAW)
 
     // ---- producer (thread 0): items in order, as long as all their slots
     // fit in the ring ahead of the released slot positions ------------------
@@ -404,7 +591,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
         // in-kernel gradients: per-element std and Student-t flags
         float stdv[SLOTS][4];
         uint32_t heavy[SLOTS];
-        if constexpr (GK == kGradPhilox) {
+        if constexpr (GK == kGradPhilox && !DRAW) {
             int l = l0;
             int64_t lend = D.layer_end[l];
 #pragma unroll
@@ -425,7 +612,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
         // this thread's elements all draw from one kind of stream (true
         // except at a boundary between a normal and a heavy-tailed tensor)
         bool all_normal = true, all_heavy = true;
-        if constexpr (GK == kGradPhilox) {
+        if constexpr (GK == kGradPhilox && !DRAW) {
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
                 all_normal = all_normal && heavy[s] == 0u;
@@ -472,13 +659,18 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             const unsigned char* a = ring + (uint32_t)cp.slot * R::kSlot;
             const void* eb = ring + (uint32_t)cp.plus(SL::kPerWorker - 1).slot * R::kSlot;
             cp = cp.plus(SL::kPerWorker);
+            if constexpr (DRAW) {
+                // this worker's gradients, written by the draw warps
+                if (!wait_handoff(&gfull[gcp.slot], gcp.phase, nullptr)) lost = true;
+                a = reinterpret_cast<const unsigned char*>(gring + gcp.slot * TILE);
+            }
             float z[SLOTS][4];
             // in-kernel gradients.  Normal elements: the draws of all slots
             // as independent Philox chains (instruction-level parallelism).
             // Heavy-tailed elements: one Student-t draw each, again as
             // independent chains when all of the thread's elements are heavy.
             float gin[SLOTS][4];
-            if constexpr (GK == kGradPhilox) {
+            if constexpr (GK == kGradPhilox && !DRAW) {
                 if (all_heavy) {
 #pragma unroll
                     for (int s = 0; s < SLOTS; ++s)
@@ -517,7 +709,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                 for (int s = 0; s < SLOTS; ++s) {
                     const int off = s * NT * 4 + tid * 4;
                     float g[4];
-                    load_grad4<GK>(a, off, gin[s], g);
+                    load_grad4<GKC>(a, off, gin[s], g);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         if (c < nv[s] && !isfinite(g[c])) bad = true;
@@ -530,7 +722,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
                 for (int s = 0; s < SLOTS; ++s) {
                     const int off = s * NT * 4 + tid * 4;
                     float g[4], ee[4];
-                    load_grad4<GK>(a, off, gin[s], g);
+                    load_grad4<GKC>(a, off, gin[s], g);
                     load_err4<EB>(eb, off, ee);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -545,7 +737,12 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             };
             if (full_tile) momentum_and_norms(std::true_type{});
             else momentum_and_norms(std::false_type{});
-            if (__syncthreads_or(lost)) goto abort;
+            if constexpr (DRAW) {
+                // every gradient of the slot has been read: hand it back
+                warp_arrive(&gempty[gcp.slot]);
+                gcp = gcp.plus(1);
+            }
+            if (sync_or<NT, DRAW>(lost)) goto abort;
             released += (w == 0) ? 1 + SL::kPerWorker : SL::kPerWorker;
             if (tid == 0) issue_ready();
             const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
@@ -615,7 +812,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             };
             if (full_tile) average_and_norms(std::true_type{});
             else average_and_norms(std::false_type{});
-            if (__syncthreads_or(lost)) goto abort;
+            if (sync_or<NT, DRAW>(lost)) goto abort;
             released += nsrv;
             if (tid == 0) issue_ready();
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
@@ -690,7 +887,7 @@ __global__ void __launch_bounds__(NT, (MinBlocks<NT, SLOTS, NSLOT>::value))
             flush_max();
             if (warp == 0 && lane_stores_scale) D.scale_s[kq] = ssq;
         }
-        __syncthreads();
+        sync_all<NT, DRAW>();
         {
             const int nl = D.chunk_l1[klast] - l0 + 1;
             for (int jj = tid; jj < nl && jj < kMaxChunkLayers; jj += NT) {
@@ -708,6 +905,7 @@ abort:
     // CTA still has in flight land (bounded), then leave.
     if (tid == 0) {
         atomicOr(D.flags, 2u);
+        if constexpr (DRAW) *(volatile int*)&stop_draw = 1;     // the draw warps leave too
         // every slot position issued but not yet released (at most NSLOT):
         // they end at the producer's position ip.  Each one whose copies were
         // issued is waited for with the default bound, whatever bound the
@@ -722,17 +920,19 @@ abort:
             wait_stage(&full[q.slot], q.phase, kDefaultWaitTries);
         }
     }
-    __syncthreads();
+    sync_all<NT, DRAW>();
 }
 
 cudaError_t launch_update(const Problem& P, const Dev& D, float* x, int msig, cudaStream_t st);
 
-template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM, bool EB>
+template <int NT, int SLOTS, int GK, int NSLOT, int C, bool ADAM, bool EB, int NDRAW = 0>
 static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     constexpr int TILE = NT * 4 * SLOTS;
-    constexpr size_t smem = (size_t)NSLOT * Ring<TILE>::kSlot;
-    auto kern = k_compress<NT, SLOTS, GK, NSLOT, C, ADAM, EB>;
+    // the copy ring, then (with draw warps) the gradient slots
+    constexpr size_t smem = (size_t)NSLOT * Ring<TILE>::kSlot
+                            + (NDRAW > 0 ? (size_t)kDrawSlots * TILE * 4 : 0);
+    auto kern = k_compress<NT, SLOTS, GK, NSLOT, C, ADAM, EB, NDRAW>;
     // Launch shape per device and instantiation, set up on first use.  A slot
     // is published only after its device's function attributes are set, and
     // concurrent first uses on one device just repeat the same settings, so
@@ -750,14 +950,14 @@ static cudaError_t launch_one(const Problem& P, const Dev& D, const Grads& G, cu
                                       cudaSharedmemCarveoutMaxShared)))
             return e;
         int per_sm = 0, sms = 0;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem))) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT + NDRAW, smem))) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
         grid_cap = (per_sm > 0 ? per_sm : 1) * sms;
         if (dev < kCachedDevices) grid_cap_of[dev].store(grid_cap, std::memory_order_release);
     }
     const int64_t ntiles = P.Np / TILE;
     const unsigned grid = (unsigned)(ntiles < grid_cap ? ntiles : grid_cap);
-    kern<<<grid, NT, smem, st>>>(P, D, G);
+    kern<<<grid, NT + NDRAW, smem, st>>>(P, D, G);
     return cudaGetLastError();
 }
 
@@ -795,6 +995,7 @@ cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads&
     case 4096:
         if constexpr (!EB)
             if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 4096, ADAM, EB>(P, D, G, st);
+        if (G.kind == kGradPhilox) return launch_one<512, 2, kGradPhilox, 7, 4096, ADAM, EB, 512>(P, D, G, st);
         return launch_grad<256, 4, 7, 4096, ADAM, EB>(P, D, G, st);
     case 8192: return launch_grad<512, 4, 7, 8192, ADAM, EB>(P, D, G, st);
     default:   return cudaErrorInvalidValue;

@@ -22,10 +22,12 @@ def dispatched_shapes():
     for m in re.finditer(r"launch_grad<(\d+), (\d+), (\d+), (\d+), ADAM, EB>", body):
         nt, slots, nslot, c = map(int, m.groups())
         for gk in (0, 1, 2):
-            shapes.add((nt, slots, nslot, c, gk))
-    for m in re.finditer(r"launch_one<(\d+), (\d+), kGrad(F32|BF16|Philox), (\d+), (\d+), ADAM, EB>", body):
-        nt, slots, kind, nslot, c = m.groups()
-        shapes.add((int(nt), int(slots), int(nslot), int(c), {"F32": 0, "BF16": 1, "Philox": 2}[kind]))
+            shapes.add((nt, slots, nslot, c, gk, 0))
+    for m in re.finditer(r"launch_one<(\d+), (\d+), kGrad(F32|BF16|Philox), (\d+), (\d+), ADAM, EB(?:, (\d+))?>",
+                         body):
+        nt, slots, kind, nslot, c, ndraw = m.groups()
+        shapes.add((int(nt), int(slots), int(nslot), int(c), {"F32": 0, "BF16": 1, "Philox": 2}[kind],
+                    int(ndraw or 0)))
     return sorted(shapes)
 
 
@@ -35,11 +37,12 @@ SHAPES = dispatched_shapes()
 def test_dispatch_table_was_parsed():
     cs = {s[3] for s in SHAPES}
     assert cs == {256, 512, 1024, 2048, 4096, 8192}
-    assert (512, 2, 7, 4096, 0) in SHAPES
+    assert (512, 2, 7, 4096, 0, 0) in SHAPES
+    assert (512, 2, 7, 4096, 2, 512) in SHAPES        # in-kernel gradients with draw warps
 
 
-@pytest.mark.parametrize("nt,slots,nslot,c,gk", SHAPES)
-def test_shape_bounds(nt, slots, nslot, c, gk):
+@pytest.mark.parametrize("nt,slots,nslot,c,gk,ndraw", SHAPES)
+def test_shape_bounds(nt, slots, nslot, c, gk, ndraw):
     tile = nt * 4 * slots
     nwarp = nt // 32
     npart = tile // 128
@@ -48,13 +51,30 @@ def test_shape_bounds(nt, slots, nslot, c, gk):
     assert nt % 32 == 0 and nt <= 1024
     assert tile % c == 0 and cpt >= 1, "a tile holds whole chunks"
     assert slots & (slots - 1) == 0 and slots <= 8, "pack_words handles up to 8 slots"
-    # ring: NSLOT slots of TILE floats; two CTAs per SM when two rings fit
+    # ring: NSLOT slots of TILE floats; two CTAs per SM when two rings fit; a
+    # CTA with draw warps adds kDrawSlots gradient tiles and runs alone
     slot_bytes = tile * 4
-    min_blocks = 2 if nslot * slot_bytes <= 112 * 1024 else 1
-    static = 2 * npart * 4 + 64 * 4 + nslot * 8            # red, lmax, mbarriers
-    assert nslot * slot_bytes + static <= SMEM_PER_BLOCK
-    assert min_blocks * (nslot * slot_bytes + static + 1024) <= SMEM_PER_SM
-    assert 65536 // (nt * min_blocks) >= 64, "the launch bound leaves at least 64 registers"
+    draw_slots = 3 if ndraw else 0
+    min_blocks = 1 if ndraw else (2 if nslot * slot_bytes <= 112 * 1024 else 1)
+    static = 2 * npart * 4 + 64 * 4 + nslot * 8 + 2 * max(draw_slots, 1) * 8 + 4   # red, lmax, mbarriers
+    dyn = (nslot + draw_slots) * slot_bytes
+    assert dyn + static <= SMEM_PER_BLOCK
+    assert min_blocks * (dyn + static + 1024) <= SMEM_PER_SM
+    threads = nt + ndraw
+    assert threads <= 1024
+    assert 65536 // (threads * min_blocks) >= 64, "the launch bound leaves at least 64 registers"
+    if ndraw:
+        assert gk == 2, "draw warps only for in-kernel gradients"
+        assert ndraw % 32 == 0 and nt % 32 == 0      # whole warps: per-warp arrivals, named barrier 1
+        pg = tile // (4 * ndraw)
+        assert pg >= 1 and pg * 4 * ndraw == tile
+        groups = set()
+        for d in range(ndraw):
+            for g in range(pg):
+                e = g * ndraw * 4 + d * 4
+                assert 0 <= e and e + 4 <= tile
+                groups.add(e)
+        assert len(groups) == tile // 4, "every group of four of the tile is drawn exactly once"
     # the 128-leaf partial of slot s, warp w is red[s * NWARP + w], in element order
     for s in range(slots):
         for w in range(nwarp):
