@@ -152,15 +152,22 @@ def profiled_instructions(workload_name):
 
 def profiled_traffic(workload_name):
     """dram bytes per launch of the fused kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"compress_kernel_{workload_name}.md")
+    summary, if it was taken on the current kernel source; else None.
+    Returns (bytes or None, a description of where the figure comes from).
+    It is not measured in this run: a DRAM-counter capture of the full-size
+    workload is not taken under the profiler (the summary scales a small
+    capture of the same kernel by the parameters processed)."""
+    rel = os.path.join("profiles", f"compress_kernel_{workload_name}.md")
+    path = os.path.join(ROOT, rel)
     if not os.path.exists(path):
-        return None
+        return None, f"no ncu summary {rel}"
     text = open(path).read()
     m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+source_sha:\s*([0-9a-f]+)", text)
-    if not m or m.group(2) != kernel_source_hash():
-        return None
-    return float(m.group(1))
+    if not m:
+        return None, f"{rel} records no traffic"
+    if m.group(2) != kernel_source_hash():
+        return None, f"{rel} was taken on kernel source {m.group(2)}, not the current {kernel_source_hash()}"
+    return float(m.group(1)), f"{rel}: ncu dram__bytes_read.sum + dram__bytes_write.sum (source {m.group(2)})"
 
 
 # ---------------------------------------------------------------------------
@@ -273,9 +280,10 @@ def max_over_ranks(value, world):
 # CPU oracle on a bounded sample (baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(wl, seconds, max_steps=None):
+def oracle_sample_rate(wl, seconds, max_steps=None, variant="lamb", errors="f32"):
     """Times the oracle's compression step on the leading chunks of the
-    workload.  Returns (elements/s, description, steps)."""
+    workload.  Returns (elements/s, description, steps, step times, sampled
+    parameters, sampled chunks)."""
     import oracle
     C, W = wl.chunk, wl.W
 
@@ -288,7 +296,8 @@ def oracle_sample_rate(wl, seconds, max_steps=None):
                 break
             frags.append((int(o), int(min(e, n) - o)))
         x0 = workload.gen_params(wl, 0, n)
-        o = oracle.Oracle([f[0] for f in frags], [f[1] for f in frags], W, C, wl.hp, x0)
+        o = oracle.Oracle([f[0] for f in frags], [f[1] for f in frags], W, C, wl.hp, x0,
+                          variant=1 if variant == "adam" else 0, err_bf16=1 if errors == "bf16" else 0)
         o.v[:] = 1e-6
         o.freeze()
         g = np.empty((W, n), np.float32)
@@ -314,7 +323,11 @@ def oracle_sample_rate(wl, seconds, max_steps=None):
     rate = n / statistics.median(times)
     desc = (f"oracle compression step on the leading {n} parameters ({nchunks} chunks of "
             f"{C}, W={W}) of {wl.name}; median of {len(times)} steps")
-    return rate, desc, len(times), times
+    return rate, desc, len(times), times, n, nchunks
+
+
+def variant_name(v):
+    return "1-bit LAMB" if v == "lamb" else "1-bit Adam"
 
 
 def cpu_info():
@@ -335,8 +348,9 @@ def run_reference(args, world, rank):
     wl = get_workload(args)
     total = max(30.0, 2.0 * (args.steps + args.warmup))
     per_step_budget = min(1.0, 120.0 / max(1, args.steps + args.warmup))
-    rate, desc, n, times = oracle_sample_rate(wl, seconds=per_step_budget * (args.steps + args.warmup),
-                                              max_steps=args.steps + args.warmup)
+    rate, desc, n, times, n_params, n_chunks = oracle_sample_rate(
+        wl, seconds=per_step_budget * (args.steps + args.warmup), max_steps=args.steps + args.warmup,
+        variant=args.variant, errors=args.errors)
     timed = times[args.warmup:] or times
     ms = 1e3 * statistics.mean(timed)
     value = rate
@@ -346,7 +360,11 @@ def run_reference(args, world, rank):
         "steps": len(timed), "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "W": wl.W, "chunk": wl.chunk, "params": wl.N,
-                   "grads": wl.grad},
+                   "tensors": wl.L, "grads": wl.grad, "variant": variant_name(args.variant),
+                   "error_storage": args.errors,
+                   # the oracle is timed on a bounded prefix of the table: the
+                   # value is a rate (parameters per second), not a full step
+                   "sampled_params": n_params, "sampled_chunks": n_chunks},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": desc, "host": arch, "host_cpus": ncpu},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -417,7 +435,7 @@ def run_ours(args, world, rank, local):
 
     # warmup stage (LAMB), timed per step for information
     t = 0
-    warm_ms, warm_kernel_ms = [], []
+    warm_ms, warm_kernel_ms, warm_layer_ms = [], [], []
     n_warm_stage = wl.warmup_steps if args.warmup_stage_steps < 0 else args.warmup_stage_steps
     for _ in range(n_warm_stage):
         regen(t)
@@ -427,6 +445,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         warm_ms.append(ev[0].elapsed_time(ev[3]))
         warm_kernel_ms.append(ev[0].elapsed_time(ev[1]))
+        warm_layer_ms.append(ev[1].elapsed_time(ev[2]))
         t += 1
     opt.freeze_variance()
     for _ in range(args.warmup):
@@ -464,12 +483,13 @@ def run_ours(args, world, rank, local):
     kb = fused_kernel_bytes(wl, args.variant, args.errors)
     k_avg = statistics.mean(kern_ms)
     achieved = kb / (k_avg / 1e3) / 1e9
-    traffic = profiled_traffic(wl.name)
+    traffic, traffic_source = profiled_traffic(wl.name)
     copy_now = live_copy_gbs()
     roofline = {"bound": "hbm", "kernel": "k_compress (fused worker+server pass)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": traffic, "alg_bytes_per_launch": kb, "kernel_ms": k_avg,
+                "traffic": traffic, "traffic_source": traffic_source,
+                "alg_bytes_per_launch": kb, "kernel_ms": k_avg,
                 "live_copy_gbs": copy_now, "frac_of_live_copy": achieved / copy_now}
     if wl.grad == "philox":
         # gradients drawn in the kernel: bound by instruction issue, not HBM
@@ -527,7 +547,7 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": wl.name, "W": W, "chunk": C, "params": N, "tensors": wl.L,
-                   "grads": wl.grad, "variant": f"1-bit {args.variant.upper() if args.variant == 'lamb' else 'Adam'}",
+                   "grads": wl.grad, "variant": variant_name(args.variant),
                    "error_storage": args.errors,
                    "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (each step moves %.1f GB); gradients regenerated "
@@ -547,6 +567,7 @@ def run_ours(args, world, rank, local):
                  "worker_elements_per_s": W * value, "wall_s": wall},
         "warmup_stage": ({"ms_per_step": statistics.mean(warm_ms[1:] or warm_ms),
                           "moments_kernel_ms": statistics.mean(warm_kernel_ms[1:] or warm_kernel_ms),
+                          "per_tensor_ms": statistics.mean(warm_layer_ms[1:] or warm_layer_ms),
                           "params_per_s": N / (statistics.mean(warm_ms[1:] or warm_ms) / 1e3),
                           "steps": len(warm_ms)} if warm_ms else None),
         "gpu_launches": (2 if args.variant == "adam" else 3) * args.steps,
@@ -555,7 +576,8 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, desc, n, _ = oracle_sample_rate(wl, seconds=args.cpu_seconds)
+        rate, desc, n, _, _, _ = oracle_sample_rate(wl, seconds=args.cpu_seconds, variant=args.variant,
+                                                    errors=args.errors)
         arch, ncpu = cpu_info()
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": desc, "host": arch, "host_cpus": ncpu}

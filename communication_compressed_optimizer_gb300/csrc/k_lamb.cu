@@ -305,8 +305,12 @@ __global__ void __launch_bounds__(kNT) k_warmup_moments(const Problem P, const D
 }
 
 // ---- per tensor: level-1 tree over granule sums, trust ratio, coefficient -----
-// Leaf j of tensor l is granule sum j = half 2j + half 2j+1; the tree over the
-// tensor's granule sums is split into 256 aligned blocks, one per thread.
+// Leaf j of tensor l is granule sum j = half 2j + half 2j+1.  The tensor's
+// level-1 tree (zero-padded to a power of two) is evaluated in two passes:
+// k_layer_blocks forms the subtrees over aligned blocks of kLevel1Block
+// leaves, many CTAs per large tensor; k_layer_finish forms the tree over a
+// tensor's block sums.  Both split their leaves into 256 aligned runs, one
+// per thread, so every partial sum is a subtree of the canonical tree.
 __device__ float block_tree256(float v, float* sh)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -324,15 +328,18 @@ __device__ float block_tree256(float v, float* sh)
     return r;   // valid in warp 0
 }
 
-// Pairwise tree over leaves leaf(j0 .. j0+B) (B a power of two), leaves past
+// Pairwise tree over leaves j0 .. j0+B (B a power of two), leaves at or past
 // cnt are +0, computed left to right with a stack of completed subtrees.
+// HALVES: leaf j is part[2j] + part[2j+1]; otherwise part[j].
+template <bool HALVES>
 __device__ float seq_tree(const float* part, int64_t j0, int64_t B, int64_t cnt)
 {
     float stk[40];
     int lvl[40];
     int sp = 0;
     for (int64_t j = j0; j < j0 + B; ++j) {
-        float v = (j < cnt) ? fadd(part[2 * j], part[2 * j + 1]) : 0.0f;
+        float v = 0.0f;
+        if (j < cnt) v = HALVES ? fadd(part[2 * j], part[2 * j + 1]) : part[j];
         int lv = 0;
         while (sp > 0 && lvl[sp - 1] == lv) { v = fadd(stk[sp - 1], v); ++lv; --sp; }
         stk[sp] = v; lvl[sp] = lv; ++sp;
@@ -340,18 +347,44 @@ __device__ float seq_tree(const float* part, int64_t j0, int64_t B, int64_t cnt)
     return stk[0];
 }
 
+// One CTA per level-1 block (tensor l, block b): the subtree over granule
+// sums b*kLevel1Block .. (b+1)*kLevel1Block of the tensor.
+__global__ void __launch_bounds__(kNT) k_layer_blocks(const Problem P, const Dev D)
+{
+    __shared__ float sh[kNT / 32];
+    constexpr int64_t kPer = kLevel1Block / kNT;      // leaves per thread
+    const int64_t blk = blockIdx.x;
+    int lo = 0, hi = P.L - 1;                          // the tensor holding this block
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (D.bbase[mid] <= blk) lo = mid; else hi = mid - 1;
+    }
+    const int l = lo;
+    const int64_t hb = D.hbase[l];
+    const int64_t cnt = (D.hbase[l + 1] - hb) / 2;
+    const int64_t j0 = (blk - D.bbase[l]) * kLevel1Block + (int64_t)threadIdx.x * kPer;
+    const float vx = seq_tree<true>(D.part_x + hb, j0, kPer, cnt);
+    const float vu = seq_tree<true>(D.part_u + hb, j0, kPer, cnt);
+    const float bx = block_tree256(vx, sh);
+    const float bu = block_tree256(vu, sh);
+    if (threadIdx.x == 0) {
+        D.blk_x[blk] = bx;
+        D.blk_u[blk] = bu;
+    }
+}
+
 __global__ void __launch_bounds__(kNT) k_layer_finish(const Problem P, const Dev D, int first_warmup)
 {
     __shared__ float sh[kNT / 32];
     const int l = blockIdx.x;
-    const int64_t hb = D.hbase[l];
-    const int64_t cnt = (D.hbase[l + 1] - hb) / 2;
+    const int64_t b0 = D.bbase[l];
+    const int64_t nb = D.bbase[l + 1] - b0;
     int64_t p2 = 1;
-    while (p2 < cnt) p2 <<= 1;
+    while (p2 < nb) p2 <<= 1;
     const int64_t B = p2 > kNT ? p2 / kNT : 1;
     const int64_t j0 = (int64_t)threadIdx.x * B;
-    const float vx = seq_tree(D.part_x + hb, j0, B, cnt);
-    const float vu = seq_tree(D.part_u + hb, j0, B, cnt);
+    const float vx = seq_tree<false>(D.blk_x + b0, j0, B, nb);
+    const float vu = seq_tree<false>(D.blk_u + b0, j0, B, nb);
     const float Sx = block_tree256(vx, sh);
     const float Su = block_tree256(vu, sh);
     if (threadIdx.x == 0) {
@@ -381,6 +414,8 @@ cudaError_t launch_warmup(const Problem& P, const Dev& D, const Grads& G, float*
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = trace(ev, 1, st)) != cudaSuccess) return e;
     if (!P.adam) {   // Adam keeps c = 1 (gc = lr from the initialisation)
+        k_layer_blocks<<<(unsigned)P.NB, kNT, 0, st>>>(P, D);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         k_layer_finish<<<(unsigned)P.L, kNT, 0, st>>>(P, D, first_warmup);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

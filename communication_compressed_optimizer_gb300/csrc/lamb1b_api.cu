@@ -22,11 +22,11 @@ namespace {
 enum Region {
     R_M, R_V, R_VF, R_DF, R_ES, R_EW, R_SW, R_SS, R_SCW, R_SCS,
     R_CBAR, R_RPREV, R_CCUR, R_GC, R_RLAST, R_SX, R_SU, R_RMAX,
-    R_LOFF, R_LEND, R_HBASE, R_CL0, R_CL1, R_PX, R_PU, R_FLAGS, R_COUNT
+    R_LOFF, R_LEND, R_HBASE, R_CL0, R_CL1, R_PX, R_PU, R_BBASE, R_BX, R_BU, R_FLAGS, R_COUNT
 };
 
 struct Plan {
-    int64_t N = 0, Np = 0, K = 0, words_ld = 0, H = 0;
+    int64_t N = 0, Np = 0, K = 0, words_ld = 0, H = 0, NB = 0;
     int32_t L = 0, W = 0, C = 0;
     size_t off[R_COUNT] = {};
     size_t total = 0;
@@ -63,15 +63,17 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     int rc = check_hparams(hp);
     if (rc) return rc;
     if (!layers || L < 1 || L > (1 << 24)) return LAMB1B_ERR_ARG;
-    int64_t N = 0, H = 0;
+    int64_t N = 0, H = 0, NB = 0;
     for (int32_t l = 0; l < L; ++l) {
         if (layers[l].offset != N || layers[l].numel < 1) return LAMB1B_ERR_ARG;
         if (layers[l].numel > (int64_t(1) << 40) - N) return LAMB1B_ERR_ARG;
         const int64_t g0 = layers[l].offset / lamb1b::kGranule;
         const int64_t g1 = (layers[l].offset + layers[l].numel - 1) / lamb1b::kGranule;
         H += 2 * (g1 - g0 + 1);
+        NB += lamb1b::level1_blocks(g1 - g0 + 1);
         N += layers[l].numel;
     }
+    if (NB > 0x7FFFFFFFll) return LAMB1B_ERR_ARG;
     p->N = N;
     p->L = L;
     p->W = hp->W;
@@ -81,6 +83,7 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     p->Np = lamb1b::padded_length(N, p->C);   // whole compression tiles
     p->words_ld = p->Np / 32;
     p->H = H;
+    p->NB = NB;
     const size_t f = sizeof(float);
     size_t bytes[R_COUNT];
     const size_t fe = hp->error_storage ? 2 : 4;   // error element size
@@ -96,6 +99,8 @@ int make_plan(const lamb1b_layer* layers, int32_t L, const lamb1b_hparams* hp, P
     bytes[R_HBASE] = sizeof(int64_t) * (L + 1);
     bytes[R_CL0] = bytes[R_CL1] = sizeof(int32_t) * p->K;
     bytes[R_PX] = bytes[R_PU] = f * H;
+    bytes[R_BBASE] = sizeof(int64_t) * (L + 1);
+    bytes[R_BX] = bytes[R_BU] = f * NB;
     bytes[R_FLAGS] = 16;
     size_t cur = 0;
     for (int r = 0; r < R_COUNT; ++r) {
@@ -126,7 +131,7 @@ struct lamb1b_ctx {
     int64_t t = 0;
     int32_t n_warm = 0;
     int32_t stage = 0;
-    std::vector<int64_t> off, end, hbase;
+    std::vector<int64_t> off, end, hbase, bbase;
     std::vector<int32_t> l0, l1;
     bool tracing = false;
     bool d_frz_valid = false;   // D.d_frz holds sqrt(v) + eps of the frozen v
@@ -263,18 +268,25 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     D.chunk_l1 = reinterpret_cast<int32_t*>(ws + p.off[R_CL1]);
     D.part_x = reinterpret_cast<float*>(ws + p.off[R_PX]);
     D.part_u = reinterpret_cast<float*>(ws + p.off[R_PU]);
+    D.bbase = reinterpret_cast<int64_t*>(ws + p.off[R_BBASE]);
+    D.blk_x = reinterpret_cast<float*>(ws + p.off[R_BX]);
+    D.blk_u = reinterpret_cast<float*>(ws + p.off[R_BU]);
+    P.NB = p.NB;
     D.flags = reinterpret_cast<uint32_t*>(ws + p.off[R_FLAGS]);
 
     // host tables
     c->off.resize(L);
     c->end.resize(L);
     c->hbase.resize(L + 1);
+    c->bbase.resize(L + 1);
     c->hbase[0] = 0;
+    c->bbase[0] = 0;
     for (int32_t l = 0; l < L; ++l) {
         c->off[l] = layers[l].offset;
         c->end[l] = layers[l].offset + layers[l].numel;
         const int64_t g0 = c->off[l] / lamb1b::kGranule, g1 = (c->end[l] - 1) / lamb1b::kGranule;
         c->hbase[l + 1] = c->hbase[l] + 2 * (g1 - g0 + 1);
+        c->bbase[l + 1] = c->bbase[l] + lamb1b::level1_blocks(g1 - g0 + 1);
     }
     c->l0.resize(p.K);
     c->l1.resize(p.K);
@@ -296,6 +308,8 @@ extern "C" int lamb1b_init(lamb1b_ctx** out, const lamb1b_layer* layers, int32_t
     ok = ok && cudaMemcpyAsync(D.layer_end, c->end.data(), sizeof(int64_t) * L,
                                cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(D.hbase, c->hbase.data(), sizeof(int64_t) * (L + 1),
+                               cudaMemcpyHostToDevice, st) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(D.bbase, c->bbase.data(), sizeof(int64_t) * (L + 1),
                                cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(D.chunk_l0, c->l0.data(), sizeof(int32_t) * p.K,
                                cudaMemcpyHostToDevice, st) == cudaSuccess;

@@ -12,6 +12,15 @@
 namespace lamb1b {
 
 constexpr int kGranule = 256;        // level-0 block of the canonical pairwise tree
+// The level-1 tree of a tensor (over its granule sums, zero-padded to a power
+// of two) is evaluated as subtrees over aligned blocks of kLevel1Block granule
+// sums, then a tree over the block sums.  All partial sums are >= +0, so a
+// subtree over a block that reaches past the padded length adds only +0.
+constexpr int64_t kLevel1Block = 4096;
+__host__ __device__ constexpr int64_t level1_blocks(int64_t granules)
+{
+    return (granules + kLevel1Block - 1) / kLevel1Block;
+}
 constexpr int kMaxChunkLayers = 64;  // per-chunk layer slots kept in shared memory
 
 // Default bound of a shared-memory copy wait, in mbarrier.try_wait calls
@@ -24,6 +33,7 @@ struct Problem {
     int64_t K;        // chunks
     int64_t words_ld; // Np / 32
     int32_t L, W, C;
+    int64_t NB;       // level-1 blocks of all tensors (warmup norms)
     float lr, beta1, beta2, eps, wd;
     float omega1, omega2;             // fl(1 - beta1), fl(1 - beta2)
     float cmin, cmax, cema, one_m_cema;
@@ -67,6 +77,9 @@ struct Dev {
     int32_t* chunk_l1;   // [K] layer of the chunk's last element
     float* part_x;       // [hbase[L]] warmup half-granule sums of x^2
     float* part_u;       // [hbase[L]] warmup half-granule sums of u^2
+    int64_t* bbase;      // [L+1] first level-1 block of each layer
+    float* blk_x;        // [NB] level-1 block sums of x^2 (kLevel1Block granule sums each)
+    float* blk_u;        // [NB] the same for u^2
     uint32_t* flags;     // [4] bit 0: non-finite gradient seen
 };
 
