@@ -980,18 +980,22 @@ template <bool ADAM, bool EB>
 cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads& G, cudaStream_t st)
 {
     // 4096-element tiles (256 threads x 4 float4 groups) holding 4096/C chunks;
-    // 8192-element chunks use 512-thread tiles of one chunk.  For C = 4096 with
-    // stored binary32 gradients and errors (a streaming-bound case) the same
-    // tile is split over 512 threads x 2 groups: 64 registers, no spills, so
+    // 8192-element chunks use 512-thread tiles of one chunk.  For C = 2048 and
+    // 4096 with stored binary32 gradients and errors (streaming-bound cases)
+    // the same tile is split over 512 threads x 2 groups: 64 registers, so
     // two CTAs give 32 warps per SM to cover the arithmetic between the
-    // barriers (BERT-Large fused kernel 11.72 -> 11.22 ms on one box).  The
-    // other cases keep 256 threads: there the wider CTA spills or, where the
-    // kernel is issue-bound (bfloat16 errors), runs slower.
+    // barriers (same-box A/B, fused kernel: BERT-Large 11.72 -> 11.22 ms,
+    // BERT-Base 2.05 -> 1.99 ms).  With bfloat16 errors the wider CTA runs
+    // 23 % slower, so those keep 256 threads.  In-kernel gradients at C = 4096
+    // add 512 draw threads (draw_gradients).
     switch (P.C) {
     case 256:  return launch_grad<256, 4, 7, 256, ADAM, EB>(P, D, G, st);
     case 512:  return launch_grad<256, 4, 7, 512, ADAM, EB>(P, D, G, st);
     case 1024: return launch_grad<256, 4, 7, 1024, ADAM, EB>(P, D, G, st);
-    case 2048: return launch_grad<256, 4, 7, 2048, ADAM, EB>(P, D, G, st);
+    case 2048:
+        if constexpr (!EB)
+            if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 2048, ADAM, EB>(P, D, G, st);
+        return launch_grad<256, 4, 7, 2048, ADAM, EB>(P, D, G, st);
     case 4096:
         if constexpr (!EB)
             if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 4096, ADAM, EB>(P, D, G, st);
