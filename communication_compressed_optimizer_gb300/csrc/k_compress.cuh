@@ -368,12 +368,14 @@ __device__ __forceinline__ void store_err4(void* base, int64_t off, const float 
     }
 }
 
-// Two CTAs per SM when two rings fit in shared memory, else one; a CTA with
-// draw warps (NDRAW > 0) runs alone on its SM.
+// CTAs per SM by the size of the copy ring: three when three rings fit in
+// shared memory, two for two, else one; a CTA with draw warps (NDRAW > 0)
+// runs alone on its SM.
 template <int NT, int SLOTS, int NSLOT, int NDRAW = 0>
 struct MinBlocks {
+    static constexpr int kRing = NSLOT * (NT * 4 * SLOTS) * 4;
     static constexpr int value =
-        NDRAW > 0 ? 1 : ((NSLOT * (NT * 4 * SLOTS) * 4 <= 112 * 1024) ? 2 : 1);
+        NDRAW > 0 ? 1 : (kRing <= 72 * 1024 ? 3 : (kRing <= 112 * 1024 ? 2 : 1));
 };
 
 // Gradient tiles in flight between the draw warps and the compressing warps.
@@ -1000,6 +1002,8 @@ cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads&
         if constexpr (!EB)
             if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 4096, ADAM, EB>(P, D, G, st);
         if (G.kind == kGradPhilox) return launch_one<512, 2, kGradPhilox, 7, 4096, ADAM, EB, 512>(P, D, G, st);
+        if constexpr (ADAM && EB)   // three CTAs per SM with a 4-slot ring (1-bit LAMB spills there)
+            if (G.kind == kGradF32) return launch_one<256, 4, kGradF32, 4, 4096, ADAM, EB>(P, D, G, st);
         return launch_grad<256, 4, 7, 4096, ADAM, EB>(P, D, G, st);
     case 8192: return launch_grad<512, 4, 7, 8192, ADAM, EB>(P, D, G, st);
     default:   return cudaErrorInvalidValue;

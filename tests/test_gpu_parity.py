@@ -160,6 +160,13 @@ def test_bf16_error_storage(variant):
     run(wl, wl.warmup_steps, wl.compress_steps, variant=variant, error_storage=1)
 
 
+@pytest.mark.parametrize("variant", [0, 1])
+def test_bf16_error_storage_4096(variant):
+    """bfloat16 errors with 4096-element chunks and W = 16 (the BERT-Large
+    shape of that option; 1-bit Adam runs it at three CTAs per SM)."""
+    run(bert_mini(W=16, chunk=4096), 4, 6, variant=variant, error_storage=1)
+
+
 def test_bf16_error_storage_with_bf16_and_in_kernel_gradients():
     t = workload.gpt2_tensors(2, 48, 192, 500, n_pos=64)
     run(workload.custom("gpt2_mini", t, W=8, chunk=8192, grad="bf16", grad_std=1e-3), 2, 3,
