@@ -499,6 +499,13 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     // in-kernel gradients drawn by dedicated warps (see draw_gradients)
     constexpr bool DRAW = GK == kGradPhilox && NDRAW > 0;
     constexpr int GKC = DRAW ? kGradF32 : GK;   // how the compressing threads read gradients
+    // Full tiles do their element-wise sums in packed pairs (f32x2.cuh; the
+    // same bits as the scalar form) where that measured faster: BERT-Base
+    // (512 x 2, C = 2048), bfloat16 errors, C = 8192 and in-kernel gradients.
+    // The 512 x 2 tile with stored gradients at C = 4096 (BERT-Large) ran
+    // 2 % slower with them (the server pass alone spilled at 64 registers)
+    // and keeps the scalar form.
+    constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox);
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;
@@ -726,13 +733,27 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
                     float g[4], ee[4];
                     load_grad4<GKC>(a, off, gin[s], g);
                     load_err4<EB>(eb, off, ee);
+                    if constexpr (FULL && PACK) {      // as below, the sums in packed pairs
+                        float t[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
-                        z[s][c] = (FULL || c < nv[s]) ? fadd(mw, ee[c]) : 0.0f;
+                        for (int c = 0; c < 4; ++c) t[c] = fmul(P.omega1, g[c]);
+                        add4(t, bm[s], t);
+                        add4(z[s], t, ee);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float mw = fadd(bm[s][c], fmul(P.omega1, g[c]));
+                            z[s][c] = (FULL || c < nv[s]) ? fadd(mw, ee[c]) : 0.0f;
+                        }
                     }
-                    part[s] = fadd(fadd(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1])),
-                                   fadd(fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3])));
+                    if constexpr (PACK) {
+                        float q[4];
+                        mul4(q, z[s], z[s]);
+                        part[s] = fadd(fadd(q[0], q[1]), fadd(q[2], q[3]));
+                    } else {
+                        part[s] = fadd(fadd(fmul(z[s][0], z[s][0]), fmul(z[s][1], z[s][1])),
+                                       fadd(fmul(z[s][2], z[s][2]), fmul(z[s][3], z[s][3])));
+                    }
                 }
                 const float t = warp_trees128<SLOTS>(part, lane);
                 if (lane < SLOTS) red[w & 1][tree_block<SLOTS>(lane) * NWARP + warp] = t;
@@ -759,16 +780,26 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
                 for (int s = 0; s < SLOTS; ++s) {
                     const float sc = (CPT == 1) ? sq : __shfl_sync(0xFFFFFFFFu, sq, qsrc[s]);
                     const float nsc = -sc;
-                    float en[4];
+                    float en[4], ssv[4];
                     nib[s] = 0u;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const bool valid = FULL || c < nv[s];
                         const bool neg = z[s][c] < 0.0f;       // +0, -0 and NaN send +1
-                        const float ss = neg ? nsc : sc;
+                        ssv[c] = neg ? nsc : sc;
                         if (!neg && valid) nib[s] |= 1u << c;
-                        en[c] = valid ? fsub(z[s][c], ss) : 0.0f;
-                        acc[s][c] = fadd(acc[s][c], ss);
+                    }
+                    if constexpr (FULL && PACK) {
+                        sub4(en, z[s], ssv);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) en[c] = (FULL || c < nv[s]) ? fsub(z[s][c], ssv[c]) : 0.0f;
+                    }
+                    if constexpr (PACK) {
+                        add4(acc[s], acc[s], ssv);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[s][c] = fadd(acc[s][c], ssv[c]);
                     }
                     store_err4<EB>(D.e_w, eoff + s * NT * 4, en);
                 }
@@ -803,11 +834,24 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
                         dz[s][0] = v.x; dz[s][1] = v.y; dz[s][2] = v.z; dz[s][3] = v.w;
                         vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
                     }
+                    if constexpr (FULL && PACK) {      // the sums in packed pairs
+                        float t[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        y[s][c] = (FULL || c < nv[s]) ? fadd(div_w(acc[s][c], P), ee[c]) : 0.0f;
-                    part[s] = fadd(fadd(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1])),
-                                   fadd(fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3])));
+                        for (int c = 0; c < 4; ++c) t[c] = div_w(acc[s][c], P);
+                        add4(y[s], t, ee);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            y[s][c] = (FULL || c < nv[s]) ? fadd(div_w(acc[s][c], P), ee[c]) : 0.0f;
+                    }
+                    if constexpr (PACK) {
+                        float q[4];
+                        mul4(q, y[s], y[s]);
+                        part[s] = fadd(fadd(q[0], q[1]), fadd(q[2], q[3]));
+                    } else {
+                        part[s] = fadd(fadd(fmul(y[s][0], y[s][0]), fmul(y[s][1], y[s][1])),
+                                       fadd(fmul(y[s][2], y[s][2]), fmul(y[s][3], y[s][3])));
+                    }
                 }
                 const float t = warp_trees128<SLOTS>(part, lane);
                 if (lane < SLOTS) red[W & 1][tree_block<SLOTS>(lane) * NWARP + warp] = t;
@@ -845,22 +889,52 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
                     const int off = s * NT * 4 + tid * 4;
                     const float ss = (CPT == 1) ? ssq : __shfl_sync(0xFFFFFFFFu, ssq, qsrc[s]);
                     const float nss = -ss;
-                    float es[4], mn[4], vf[4];
+                    float es[4], mn[4], vf[4], den[4];
                     nib[s] = 0u;
+                    constexpr bool PK = FULL && PACK;
+                    if constexpr (PK) {
+                        // the per-element formulas below, in packed pairs
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const bool neg = y[s][c] < 0.0f;
+                            mn[c] = neg ? nss : ss;
+                            if (!neg) nib[s] |= 1u << c;
+                        }
+                        sub4(es, y[s], mn);
+                        if constexpr (!ADAM) {
+                            float dm[4], gt[4], t1[4], t2[4];
+                            sub4(dm, mn, bm[s]);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) gt[c] = fdiv(dm[c], P.omega1);
+                            mul4(t1, gt, gt);
+                            mul4s(t1, P.omega2, t1);
+                            mul4s(t2, P.beta2, vfo[s]);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) vf[c] = fadd(t2[c], t1[c]);   // products: scalar sums
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) t1[c] = fsqrt(vf[c]);
+                            add4s(den, t1, P.eps);
+                        }
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const bool valid = FULL || c < nv[s];
-                        const bool neg = y[s][c] < 0.0f;
-                        const float sgn = neg ? nss : ss;
-                        if (!neg && valid) nib[s] |= 1u << c;
-                        es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
-                        mn[c] = valid ? sgn : 0.0f;
+                        if constexpr (!PK) {
+                            const bool neg = y[s][c] < 0.0f;
+                            const float sgn = neg ? nss : ss;
+                            if (!neg && valid) nib[s] |= 1u << c;
+                            es[c] = valid ? fsub(y[s][c], sgn) : 0.0f;
+                            mn[c] = valid ? sgn : 0.0f;
+                        }
                         if constexpr (ADAM) continue;
-                        // reconstructed gradient and fresh second moment
-                        const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
-                        vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
+                        if constexpr (!PK) {
+                            // reconstructed gradient and fresh second moment
+                            const float gt = fdiv(fsub(mn[c], bm[s][c]), P.omega1);
+                            vf[c] = valid ? fadd(fmul(P.beta2, vfo[s][c]), fmul(P.omega2, fmul(gt, gt))) : 0.0f;
+                            den[c] = fadd(fsqrt(vf[c]), P.eps);
+                        }
                         if (valid) {
-                            float rho = fdiv(dz[s][c], fadd(fsqrt(vf[c]), P.eps));
+                            float rho = fdiv(dz[s][c], den[c]);
                             if (rho != rho) rho = __int_as_float(0x7F800000);
                             if constexpr (!ONE) {
                                 const int64_t i = base + off + c;

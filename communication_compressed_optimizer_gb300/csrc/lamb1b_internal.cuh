@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "f32x2.cuh"
 #include "philox.cuh"
 
 namespace lamb1b {
