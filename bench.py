@@ -128,7 +128,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha1()
-    for f in ("k_compress.cuh", "k_compress.cu", "lamb1b_internal.cuh", "philox.cuh"):
+    for f in ("k_compress.cuh", "k_compress.cu", "lamb1b_internal.cuh", "philox.cuh", "f32x2.cuh"):
         with open(os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -167,7 +167,9 @@ def profiled_traffic(workload_name):
         return None, f"{rel} records no traffic"
     if m.group(2) != kernel_source_hash():
         return None, f"{rel} was taken on kernel source {m.group(2)}, not the current {kernel_source_hash()}"
-    return float(m.group(1)), f"{rel}: ncu dram__bytes_read.sum + dram__bytes_write.sum (source {m.group(2)})"
+    return float(m.group(1)), (f"{rel}: ncu dram__bytes_read.sum + dram__bytes_write.sum of a smaller "
+                               f"case of the same kernel, scaled by parameters to a full launch "
+                               f"(kernel source {m.group(2)})")
 
 
 # ---------------------------------------------------------------------------
