@@ -243,6 +243,18 @@ __device__ __forceinline__ bool wait_handoff(uint64_t* bar, uint32_t parity, vol
     return false;
 }
 
+// The same wait for a whole warp (the draw warps, all 32 lanes active):
+// every decision is a warp vote, so the lanes always leave together -- none
+// can go on to the warp's __syncwarp while another has returned.
+__device__ __forceinline__ bool wait_handoff_warp(uint64_t* bar, uint32_t parity, volatile int* stop)
+{
+    for (uint32_t it = 0; it < kDefaultWaitTries; ++it) {
+        if (__all_sync(0xFFFFFFFFu, tma::try_wait(bar, parity))) return true;
+        if ((it & 255u) == 255u && __any_sync(0xFFFFFFFFu, *stop != 0)) return false;
+    }
+    return false;
+}
+
 // CTA barriers of the compressing threads.  With draw warps (DRAW) those are
 // the first NT threads only, synchronised on named barrier 1; otherwise the
 // whole CTA on barrier 0.
@@ -435,7 +447,7 @@ __device__ __forceinline__ void draw_gradients(const Problem& P, const Dev& D, c
         for (int w = 0; w < P.W; ++w) {
             // wait until the compressing threads have read this slot's last
             // tile (a fresh slot passes at once); leave if they stopped
-            if (!wait_handoff(&gempty[gp.slot], gp.phase ^ 1u, stop)) {
+            if (!wait_handoff_warp(&gempty[gp.slot], gp.phase ^ 1u, stop)) {
                 if (!*stop) atomicOr(D.flags, 2u);
                 return;
             }

@@ -153,6 +153,53 @@ def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers():
         assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
 
 
+def test_copy_wait_timeout_with_draw_warps_recovers():
+    """The same failure path in the in-kernel-gradient kernel (C = 4096: 512
+    compressing threads plus 512 draw threads per CTA).  When the first CTA's
+    compressing threads give up on a left-out copy they tell its draw warps
+    to stop, so the CTA leaves instead of waiting; the step reports
+    LAMB1B_ERR_TIMEOUT, and a restored checkpoint continues bit for bit.
+    Skipped copies: the first tile's momentum, a worker's error, the server
+    error, the fresh second moment."""
+    t = workload.bert_tensors(1, 128, 512, 800)
+    wl = workload.custom("w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
+                         fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
+    ld = grad_ld(wl)
+    ref, xr = _run_gpu_only(wl, 2, 4)
+    a, xa = _run_gpu_only(wl, 2, 2)
+    sa = a.state()
+    saved = {k: v.clone() for k, v in sa.items() if isinstance(v, torch.Tensor)}
+    counters = (sa["t"], sa["n_warmup"], sa["stage"])
+    x_saved = xa.clone()
+    t0 = counters[0]
+    W = wl.W
+    # copy positions of the first tile (gradients are drawn, not copied): 0
+    # momentum, 1 + w worker w's error, 1 + W server error, 2 + W frozen
+    # preconditioner, 3 + W fresh second moment
+    for skip in (0, 5, 1 + W, 3 + W):
+        a.set_fault_injection(skip, 2000)
+        a.compress_step(device_grads(wl, t0, ld))
+        with pytest.raises(pkg.Lamb1bError) as e:
+            a.check_status()
+        assert e.value.code == _abi.ERR_TIMEOUT, skip
+        a.check_status()
+        cur = a.state()
+        for k, v in saved.items():
+            cur[k].copy_(v)
+        xa.copy_(x_saved)
+        a.set_counters(*counters)
+    a.set_fault_injection(-1, 0)
+    for step in range(2):
+        a.compress_step(device_grads(wl, t0 + step, ld))
+    a.check_status()
+    torch.cuda.synchronize()
+    assert torch.equal(xa.view(torch.int32), xr.view(torch.int32))
+    sr, sb = ref.state(), a.state()
+    for k in ("m", "v_fresh", "e_s", "e_w", "signs_w", "signs_s", "scale_w", "scale_s",
+              "r_prev", "c_cur"):
+        assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
+
+
 def test_compress_step_replays_from_a_cuda_graph():
     """A compression step only enqueues kernels on the caller's stream (no
     host synchronisation, no allocation), so it can be captured once in a
