@@ -22,7 +22,7 @@ EXPORTED = ("lamb1b_workspace_bytes", "lamb1b_init", "lamb1b_warmup_step",
             "lamb1b_set_counters", "lamb1b_check_status", "lamb1b_set_trace_events",
             "lamb1b_set_fault_injection", "lamb1b_sync_momentum", "lamb1b_destroy",
             "lamb1b_error_string", "lamb1b_gen_grads", "lamb1b_gen_params",
-            "lamb1b_tensor_sumsq_noalloc")
+            "lamb1b_gen_selfcheck", "lamb1b_tensor_sumsq_noalloc")
 
 
 class Layer(ctypes.Structure):
@@ -96,6 +96,7 @@ def load(build_if_missing: bool = False):
     L.lamb1b_error_string.restype = ctypes.c_char_p
     L.lamb1b_gen_grads.argtypes = [_P, i64, i32, i32, u64, i64, _P, _P, i32, _P, _P, f32, _P]
     L.lamb1b_gen_params.argtypes = [_P, i64, i64, f32, u64, _P]
+    L.lamb1b_gen_selfcheck.argtypes = [_P, u64, _P]
     L.lamb1b_tensor_sumsq_noalloc.argtypes = [_P, ctypes.POINTER(Layer), i32, _P, _P]
     for f in EXPORTED:
         if f not in ("lamb1b_workspace_bytes", "lamb1b_error_string"):

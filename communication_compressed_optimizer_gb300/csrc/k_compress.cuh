@@ -513,11 +513,12 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     constexpr int GKC = DRAW ? kGradF32 : GK;   // how the compressing threads read gradients
     // Full tiles do their element-wise sums in packed pairs (f32x2.cuh; the
     // same bits as the scalar form) where that measured faster: BERT-Base
-    // (512 x 2, C = 2048), bfloat16 errors, C = 8192 and in-kernel gradients.
-    // The 512 x 2 tile with stored gradients at C = 4096 (BERT-Large) ran
-    // 2 % slower with them (the server pass alone spilled at 64 registers)
-    // and keeps the scalar form.
-    constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox);
+    // (512 x 2, C = 2048), bfloat16 errors, C = 8192, and 1-bit Adam with
+    // in-kernel gradients.  The 512 x 2 tiles at C = 4096 otherwise keep the
+    // scalar form: with stored gradients (BERT-Large) the packed sums ran 2 %
+    // slower (the server pass alone spilled at 64 registers), and 1-bit LAMB
+    // with draw warps spills less without them (54.6 against 56.3 ms).
+    constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096) || (GK == kGradPhilox && ADAM);
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;

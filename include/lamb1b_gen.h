@@ -6,7 +6,8 @@
  * tests can run at full size without host traffic.  The same definition is
  * used for gradients drawn inside the optimizer kernels (LAMB1B_GRAD_PHILOX).
  *
- * Definition (binary32, one rounding per operation, no fused multiply-add):
+ * Definition (binary32, one rounding per operation, no fused multiply-add;
+ * how the device evaluates it without changing a bit: lamb1b_gen_selfcheck):
  *   key = (seed lo32, seed hi32); Philox4x32-10 (Salmon et al., "Parallel
  *   random numbers: as easy as 1, 2, 3", SC'11).
  *   uniform(u) = (2*(u >> 9) + 1) * 2^-24.
@@ -48,6 +49,25 @@ int lamb1b_gen_grads(void* out_dev, int64_t ld, int32_t W, int32_t bf16,
 /* out_dev[j] = parameter lo + j for j in [0, hi - lo). */
 int lamb1b_gen_params(float* out_dev, int64_t lo, int64_t hi, float std,
                       uint64_t seed, void* stream);
+
+/* Self-check of how the device evaluates the definition above (a testing
+ * hook; no counterpart in the paper).  The device transform packs pairs of
+ * binary32 operations into one instruction and computes its divisions by
+ * (f+1) and by 3 and its square roots with Markstein's method (approximate
+ * reciprocal or reciprocal square root, one Newton-Raphson step, a final
+ * correction from the exact remainder), which give the IEEE result on the
+ * inputs the transform can produce.  This call enumerates those inputs and
+ * writes five mismatch counts (0 means exact) to counts_dev (caller-owned
+ * device memory, 5 x uint64, 8-byte aligned; zeroed by the call):
+ *   [0] all 2^23 log-series quotients (f-1)/(f+1);
+ *   [1] x / 3 for every non-negative binary32 x;
+ *   [2] sqrt(x) for every binary32 x >= 2^-102 (the transform's square
+ *       roots see x >= 1.19e-7 and, in Student-t, x >= 1.6e-20);
+ *   [3] the four normals of 2^22 Philox counters against the same draws
+ *       written with the IEEE intrinsics one operation at a time;
+ *   [4] the Student-t values of 2^22 elements, likewise.
+ * Takes a fraction of a second.  Errors: ARG, ALIGN, CUDA. */
+int lamb1b_gen_selfcheck(unsigned long long* counts_dev, uint64_t seed, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,5 +1,7 @@
 """GPU: on-device generator equals the host generator bit for bit;
 determinism; checkpoint/resume; non-finite detection; call-order errors."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -48,6 +50,19 @@ def test_device_philox_stream_many_counters():
     wl.seed = 12345
     want = workload.gen_grads(wl, 3, 0)
     np.testing.assert_array_equal(out.cpu().numpy()[0].view(np.uint32), want.view(np.uint32))
+
+
+def test_device_transform_division_and_square_root_are_exact():
+    """The device transform's divisions by (f+1) and by 3 and its square
+    roots (Markstein's method) give the IEEE results on every input the
+    transform can produce, enumerated completely by lamb1b_gen_selfcheck; its
+    packed normals and Student-t values equal the plain one-operation-at-a-time
+    evaluation over 2^22 counters."""
+    counts = torch.full((5,), -1, dtype=torch.int64, device="cuda")
+    rc = _abi.load().lamb1b_gen_selfcheck(ctypes.c_void_p(counts.data_ptr()), 2718,
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, _abi.load().lamb1b_error_string(rc)
+    assert counts.cpu().tolist() == [0, 0, 0, 0, 0]
 
 
 def _bert_mini(W=4, chunk=1024):
