@@ -296,6 +296,23 @@ __device__ __forceinline__ bool wait_slots(uint64_t* full, RingPos<NSLOT> p, int
     return ok;
 }
 
+// Chunk scale sqrt(S / n).  For a full chunk n = C = 2^log2c, and S / C is
+// one multiplication by 2^-log2c (both round the same real number).  The
+// square root of a finite value >= 2^-102 uses the generator's sqrt_big, which
+// gives the IEEE result on that whole range (lamb1b_gen_selfcheck enumerates
+// it); smaller values, zero, infinity, NaN and tail chunks take the rounded
+// intrinsics.
+template <int C, bool FAST>
+__device__ __forceinline__ float chunk_scale(float S, float n)
+{
+    if (FAST && n == (float)C) {
+        constexpr float kInvC = 1.0f / (float)C;       // exact: C is a power of two
+        const float m = fmul(S, kInvC);
+        return (m >= 0x1p-102f && m <= 0x1.fffffep+127f) ? gen::sqrt_big(m) : fsqrt(m);
+    }
+    return n > 0.0f ? fsqrt(fdiv(S, n)) : 0.0f;
+}
+
 // Chunk totals from the tile's 128-leaf partials red[0 .. NPART) (element
 // order).  Each lane loads G = min(4, PPC) consecutive partials with one
 // vector load and adds them as the canonical tree does (the level-2 subtrees
@@ -519,6 +536,10 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     // slower (the server pass alone spilled at 64 registers), and 1-bit LAMB
     // with draw warps spills less without them (54.6 against 56.3 ms).
     constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096) || (GK == kGradPhilox && ADAM);
+    // The chunk scale's shortcut (chunk_scale) measured faster everywhere
+    // but in that BERT-Large instantiation (3 % slower there), which keeps the
+    // plain division and square root.
+    constexpr bool FAST_SCALE = !(NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox);
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;
@@ -782,7 +803,7 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
             released += (w == 0) ? 1 + SL::kPerWorker : SL::kPerWorker;
             if (tid == 0) issue_ready();
             const float Sq = chunk_totals<NPART, PPC>(red[w & 1], lane);
-            const float sq = nq > 0.0f ? fsqrt(fdiv(Sq, nq)) : 0.0f;
+            const float sq = chunk_scale<C, FAST_SCALE>(Sq, nq);
             // this thread's error elements, and the sign words its lane stores
             const int64_t eoff = (int64_t)w * P.Np + base + tid * 4;
             uint32_t* sw = D.signs_w + (int64_t)w * P.words_ld + (base + warp * 128) / 32 + (lane >> 3);
@@ -875,7 +896,7 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
             released += nsrv;
             if (tid == 0) issue_ready();
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
-            const float ssq = nq > 0.0f ? fsqrt(fdiv(SSq, nq)) : 0.0f;
+            const float ssq = chunk_scale<C, FAST_SCALE>(SSq, nq);
 
             // Per-tensor max of rho: a running max per thread, flushed into the
             // tile's shared per-tensor slots (or global, past kMaxChunkLayers)
