@@ -35,6 +35,12 @@ PLANS = {
     "large": dict(n_warm=10, n_comp=100, checkpoints=(9, "freeze", 10, 19, 109)),
     "large_w32": dict(n_warm=50, n_comp=50, checkpoints=(48, 49, "freeze", 50, 51, 99)),
     "gpt2xl": dict(n_warm=10, n_comp=50, checkpoints=(9, "freeze", 10, 19, 59)),
+    # the options on the BERT-Large table: bfloat16 error storage with each
+    # method variant (variant 1 = 1-bit Adam)
+    "large:adam+bf16err": dict(n_warm=10, n_comp=20, checkpoints=(9, "freeze", 10, 29),
+                               variant=1, error_storage=1),
+    "large:bf16err": dict(n_warm=10, n_comp=20, checkpoints=(9, "freeze", 10, 29),
+                          error_storage=1),
 }
 
 # sampled elements per workload (bounds the oracle's CPU time), and the
@@ -116,9 +122,11 @@ def run_table(wl, k0, k1):
 
 
 def plan(name: str):
-    """The named workload, its covered tensors and its runs."""
-    wl = workload.workloads()[name]
-    return (wl,) + plan_for(wl, SAMPLE_ELEMS[name], BIG[name])
+    """The named workload (a plan name "workload:options" uses the workload
+    before the colon), its covered tensors and its runs."""
+    base = name.split(":")[0]
+    wl = workload.workloads()[base]
+    return (wl,) + plan_for(wl, SAMPLE_ELEMS[base], BIG[base])
 
 
 def plan_for(wl, max_elems: int, big: int):
@@ -171,7 +179,8 @@ def oracle_runs(wl, runs, pl, run_ids):
         k0, k1 = runs[r]
         lo, hi, frags = run_table(wl, k0, k1)
         x0 = workload.gen_params(wl, lo, hi)
-        o = oracle.Oracle([f[1] for f in frags], [f[2] for f in frags], wl.W, wl.chunk, wl.hp, x0)
+        o = oracle.Oracle([f[1] for f in frags], [f[2] for f in frags], wl.W, wl.chunk, wl.hp, x0,
+                          variant=pl.get("variant", 0), err_bf16=pl.get("error_storage", 0))
         orcs[r] = (o, lo, hi, frags)
     out = {r: {"steps": [], "checkpoints": {}} for r in run_ids}
     for step in range(n_warm + n_comp):

@@ -20,17 +20,19 @@ def _mini(W=4, chunk=512, grad="f32", heavy_every=0):
                            fan_in_scaled=True, heavy_every=heavy_every)
 
 
-@pytest.mark.parametrize("kind", ["f32", "bf16", "heavy"])
+@pytest.mark.parametrize("kind", ["f32", "bf16", "heavy", "adam+bf16err", "bf16err"])
 def test_sampled_runs_reproduce_the_whole_table(kind):
     wl = _mini(grad="bf16" if kind == "bf16" else "f32", heavy_every=5 if kind == "heavy" else 0)
     assert wl.N % 32 != 0 and wl.N % wl.chunk != 0
     tensors, runs = fullrun.plan_for(wl, max_elems=12 * wl.chunk, big=1 << 14)
     assert len(runs) >= 3 and len(tensors) >= 8
     assert runs[-1][1] == wl.K - 1                 # the ragged last chunk is sampled
-    pl = dict(n_warm=3, n_comp=4, checkpoints=(2, "freeze", 3, 6))
+    opts = dict(variant=int(kind.startswith("adam")), error_storage=int(kind.endswith("bf16err")))
+    pl = dict(n_warm=3, n_comp=4, checkpoints=(2, "freeze", 3, 6), **opts)
 
     # whole table
-    full = oracle.Oracle(wl.offsets, wl.numels, wl.W, wl.chunk, wl.hp, workload.gen_params(wl))
+    full = oracle.Oracle(wl.offsets, wl.numels, wl.W, wl.chunk, wl.hp, workload.gen_params(wl),
+                         variant=opts["variant"], err_bf16=opts["error_storage"])
     steps, cps = [], {}
     for step in range(pl["n_warm"] + pl["n_comp"]):
         if step == pl["n_warm"]:

@@ -2,7 +2,9 @@
 C=2048, 10 warmup + 10 compression steps), BERT-Large (W=16, C=4096, 10 +
 100), BERT-Large with 32 workers and in-kernel gradients (50 + 50: the
 warmup-to-compression switch at step 50) and GPT-2-XL with bfloat16
-gradients (W=8, C=8192, 10 + 50).
+gradients (W=8, C=8192, 10 + 50); and on the BERT-Large table the two
+options that select other kernel shapes, bfloat16 error storage with 1-bit
+LAMB and with 1-bit Adam (10 + 20 each).
 
 The GPU runs every step of the configuration from the seeded initial
 parameters, through the real variance freeze and the first compression
@@ -58,7 +60,8 @@ def _gpu_run(wl, runs, pl):
 
     x = torch.empty(N, device="cuda")
     pkg.gen_params(x, 0, N, wl.param_std, wl.seed)
-    opt = pkg.OneBitLamb(x, layers_of(wl), W, C, **wl.hp)
+    opt = pkg.OneBitLamb(x, layers_of(wl), W, C, **dict(wl.hp, variant=pl.get("variant", 0),
+                                                          error_storage=pl.get("error_storage", 0)))
     if wl.grad == "philox":
         g = pkg.PhiloxGrads(wl.seed, wl.layer_std, wl.layer_heavy, wl.heavy_scale)
     else:
@@ -69,9 +72,11 @@ def _gpu_run(wl, runs, pl):
 
     def snapshot():
         s = opt.state()                         # dense m brought up to date
+        # error buffers widened to binary32 (exact for bfloat16 storage)
         return dict(x=x[it_e].cpu().numpy(), m=s["m"][it_e].cpu().numpy(),
                     v=s["v"][it_e].cpu().numpy(), v_fresh=s["v_fresh"][it_e].cpu().numpy(),
-                    e_s=s["e_s"][it_e].cpu().numpy(), e_w=s["e_w"][:, it_e].cpu().numpy())
+                    e_s=s["e_s"][it_e].float().cpu().numpy(),
+                    e_w=s["e_w"][:, it_e].float().cpu().numpy())
 
     steps, cps = [], {}
     n_warm, n_comp = pl["n_warm"], pl["n_comp"]
@@ -120,7 +125,8 @@ def _close_per_frag(a, b, frags, tol):
     return True, None
 
 
-@pytest.mark.parametrize("name", ["base", "large", "large_w32", "gpt2xl"])
+@pytest.mark.parametrize("name", ["base", "large", "large_w32", "gpt2xl", "large:adam+bf16err",
+                                  "large:bf16err"])
 def test_full_size_whole_run(name):
     wl, tensors, runs = fullrun.plan(name)
     pl = fullrun.PLANS[name]
