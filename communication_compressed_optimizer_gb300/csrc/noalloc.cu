@@ -162,6 +162,15 @@ extern "C" int lamb1b_tensor_sumsq_noalloc(const float* x_dev, const lamb1b_laye
     if (!x_dev || !out_dev || !layers || L < 1) return LAMB1B_ERR_ARG;
     if (L > kMaxLayers) return LAMB1B_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(x_dev) & 15u) return LAMB1B_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the tables are staged from host memory local to this call, which a
+    // captured graph could not replay: refuse a capturing stream
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return LAMB1B_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return LAMB1B_ERR_ARG;
     if (!lamb1b::is_current_device_ptr(x_dev) || !lamb1b::is_current_device_ptr(out_dev))
         return LAMB1B_ERR_ARG;
     std::vector<int64_t> tab(3 * (size_t)L + 1);
@@ -183,7 +192,6 @@ extern "C" int lamb1b_tensor_sumsq_noalloc(const float* x_dev, const lamb1b_laye
     Scratch* S = nullptr;
     int rc = scratch_on_current_device(&S);
     if (rc) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // tables, then zeros in every half-granule slot a tensor could read
     if (cudaMemcpyAsync(S->off, off, sizeof(int64_t) * L, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(S->end, end, sizeof(int64_t) * L, cudaMemcpyHostToDevice, st) != cudaSuccess ||

@@ -303,8 +303,10 @@ int lamb1b_set_fault_injection(lamb1b_ctx* ctx, int32_t skip_copy, uint32_t wait
  * 256-element granule a tensor meets, so N up to about 5.3e8); larger inputs
  * return LAMB1B_ERR_ARG without touching the GPU.
  * The first call on a device looks up the scratch array's device address for
- * that device (make that first call before any stream capture); later calls
- * reuse it.  Every call reuses the same scratch, which keeps the previous
+ * that device; later calls reuse it.  The call stages its tables from host
+ * memory that lives only for the call, so it cannot be captured into a CUDA
+ * graph: on a stream that is capturing it returns LAMB1B_ERR_ARG and enqueues
+ * nothing.  Every call reuses the same scratch, which keeps the previous
  * call's contents; the call clears what it needs.  Calls that overlap on the
  * GPU (different streams, or different host threads) race on the scratch:
  * serialise them.  The host table is staged before the call returns.

@@ -120,3 +120,24 @@ def test_noalloc_rejects_inputs_beyond_its_limits():
     assert rc == _abi.ERR_ARG
     rc, _ = noalloc_sumsq(x[1:], [(0, 8)])                         # misaligned vector
     assert rc == _abi.ERR_ALIGN
+
+
+def test_noalloc_refuses_a_capturing_stream():
+    """The tables are staged from host memory local to the call, which a
+    graph replay could not read: under stream capture the call returns
+    LAMB1B_ERR_ARG and enqueues nothing."""
+    x = torch.ones(1024, device="cuda")
+    out = torch.full((1,), -1.0, device="cuda")
+    arr = pkg._layers_array([(0, 1024)])
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    rcs = []
+    with torch.cuda.graph(graph, stream=s):
+        rcs.append(_abi.load().lamb1b_tensor_sumsq_noalloc(
+            ctypes.c_void_p(x.data_ptr()), arr, 1, ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(s.cuda_stream)))
+    assert rcs == [_abi.ERR_ARG]
+    torch.cuda.synchronize()
+    assert out.item() == -1.0
+    rc, got = noalloc_sumsq(x, [(0, 1024)])       # the same call outside a capture
+    assert rc == 0 and got.item() == 1024.0
