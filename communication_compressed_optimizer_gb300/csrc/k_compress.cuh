@@ -540,6 +540,12 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     // but in that BERT-Large instantiation (3 % slower there), which keeps the
     // plain division and square root.
     constexpr bool FAST_SCALE = !(NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox);
+    // With three CTAs per SM (80 registers a thread), 1-bit LAMB's server
+    // pass reads the frozen preconditioner and the old fresh variance from
+    // the ring after its chunk-norm barrier instead of holding them in
+    // registers across it (which spilled), and releases those two slots at
+    // the end of the tile.
+    constexpr bool LATE = !ADAM && MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3;
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
                     const int off = s * NT * 4 + tid * 4;
                     float ee[4];
                     load_err4<EB>(es_in, off, ee);
-                    if constexpr (!ADAM) {
+                    if constexpr (!ADAM && !LATE) {
                         const float4 v = *reinterpret_cast<const float4*>(d_in + off);
                         const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
                         dz[s][0] = v.x; dz[s][1] = v.y; dz[s][2] = v.z; dz[s][3] = v.w;
@@ -893,7 +899,7 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
             if (full_tile) average_and_norms(std::true_type{});
             else average_and_norms(std::false_type{});
             if (sync_or<NT, DRAW>(lost)) goto abort;
-            released += nsrv;
+            released += LATE ? 1 : nsrv;
             if (tid == 0) issue_ready();
             const float SSq = chunk_totals<NPART, PPC>(red[W & 1], lane);
             const float ssq = chunk_scale<C, FAST_SCALE>(SSq, nq);
@@ -925,6 +931,12 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
                     const float nss = -ss;
                     float es[4], mn[4], vf[4], den[4];
                     nib[s] = 0u;
+                    if constexpr (LATE) {
+                        const float4 v = *reinterpret_cast<const float4*>(d_in + off);
+                        const float4 f = *reinterpret_cast<const float4*>(vf_in + off);
+                        dz[s][0] = v.x; dz[s][1] = v.y; dz[s][2] = v.z; dz[s][3] = v.w;
+                        vfo[s][0] = f.x; vfo[s][1] = f.y; vfo[s][2] = f.z; vfo[s][3] = f.w;
+                    }
                     constexpr bool PK = FULL && PACK;
                     if constexpr (PK) {
                         // the per-element formulas below, in packed pairs
@@ -998,6 +1010,10 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
             if (warp == 0 && lane_stores_scale) D.scale_s[kq] = ssq;
         }
         sync_all<NT, DRAW>();
+        if constexpr (LATE) {                      // the server's last two slots
+            released += 2;
+            if (tid == 0) issue_ready();
+        }
         {
             const int nl = D.chunk_l1[klast] - l0 + 1;
             for (int jj = tid; jj < nl && jj < kMaxChunkLayers; jj += NT) {
@@ -1096,8 +1112,10 @@ cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads&
     // two CTAs give 32 warps per SM to cover the arithmetic between the
     // barriers (same-box A/B, fused kernel: BERT-Large 11.72 -> 11.22 ms,
     // BERT-Base 2.05 -> 1.99 ms).  With bfloat16 errors the wider CTA runs
-    // 23 % slower, so those keep 256 threads.  In-kernel gradients at C = 4096
-    // add 512 draw threads (draw_gradients).
+    // 23 % slower, so those keep 256 threads, and at C = 4096 run three CTAs
+    // per SM with a 4-slot ring (1-bit LAMB reading its server inputs late:
+    // BERT-Large fused kernel 8.55 -> 7.71 ms, same box).  In-kernel gradients
+    // at C = 4096 add 512 draw threads (draw_gradients).
     switch (P.C) {
     case 256:  return launch_grad<256, 4, 7, 256, ADAM, EB>(P, D, G, st);
     case 512:  return launch_grad<256, 4, 7, 512, ADAM, EB>(P, D, G, st);
@@ -1110,7 +1128,7 @@ cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads&
         if constexpr (!EB)
             if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 4096, ADAM, EB>(P, D, G, st);
         if (G.kind == kGradPhilox) return launch_one<512, 2, kGradPhilox, 7, 4096, ADAM, EB, 512>(P, D, G, st);
-        if constexpr (ADAM && EB)   // three CTAs per SM with a 4-slot ring (1-bit LAMB spills there)
+        if constexpr (EB)           // three CTAs per SM with a 4-slot ring
             if (G.kind == kGradF32) return launch_one<256, 4, kGradF32, 4, 4096, ADAM, EB>(P, D, G, st);
         return launch_grad<256, 4, 7, 4096, ADAM, EB>(P, D, G, st);
     case 8192: return launch_grad<512, 4, 7, 8192, ADAM, EB>(P, D, G, st);

@@ -144,3 +144,85 @@ def test_shape_bounds(nt, slots, nslot, c, gk, ndraw):
             sbytes = ((k0 - ka + cpt) * 4 + 15) // 16 * 16
             assert ka + sbytes // 4 <= k + 16, (n, t)
             assert tile // 8 + sbytes <= slot_bytes
+
+
+def _ring_schedule(W, nslot, adam, late, ntiles):
+    """The fused kernel's copy-ring schedule, restated: thread 0 issues items
+    in order while their slots fit ahead of the released positions; the
+    compressing threads wait for an item's slots, and release them after the
+    barrier that follows their last read.  Items per tile: M (1 slot), W
+    workers (gradients + errors, 2 slots each), the server's S (errors, and
+    for 1-bit LAMB the frozen preconditioner: 1 or 2 slots) and, for 1-bit
+    LAMB, F (old fresh variance, 1 slot).  With late server reads the
+    preconditioner and F slots are released only at the end of the tile.
+    Returns the number of waits; fails if a wait is for slots not yet issued
+    (the kernel would wait for a copy that no thread will issue) or a slot is
+    released before it was read."""
+    kserver = 1 if adam else 2
+    n_items = W + (2 if adam else 3)
+
+    def slots(r):
+        return 1 if r == 0 else (2 if r <= W else (kserver if r == W + 1 else 1))
+
+    st = dict(issue_pos=0, released=0, tile=0, r=0, cp=0, waits=0)
+
+    def issue_ready():
+        while st["tile"] < ntiles:
+            n = slots(st["r"])
+            if st["issue_pos"] + n > st["released"] + nslot:
+                break
+            st["issue_pos"] += n
+            st["r"] += 1
+            if st["r"] == n_items:
+                st["r"], st["tile"] = 0, st["tile"] + 1
+
+    def wait(n):
+        assert st["cp"] + n <= st["issue_pos"], "waits for slots no thread will issue"
+        st["cp"] += n
+        st["waits"] += 1
+
+    def release(n):
+        st["released"] += n
+        assert st["released"] <= st["cp"], "released before it was read"
+        issue_ready()
+
+    issue_ready()
+    for _ in range(ntiles):
+        wait(1)                                         # M
+        for w in range(W):
+            wait(2)
+            release(3 if w == 0 else 2)                 # after the worker's barrier
+        nsrv = kserver + (0 if adam else 1)
+        wait(nsrv)
+        release(1 if late else nsrv)                    # after the server's barrier
+        if late:
+            release(2)                                  # end of the tile
+    assert st["released"] == st["cp"] == st["issue_pos"]
+    return st["waits"]
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 16, 32])
+@pytest.mark.parametrize("nslot,adam,late", [(7, False, False), (7, True, False), (4, True, False),
+                                             (4, False, True), (4, False, False)])
+def test_ring_schedule_never_waits_for_an_unissued_copy(W, nslot, adam, late):
+    assert _ring_schedule(W, nslot, adam, late, ntiles=5) == 5 * (W + 2)
+
+
+def test_ring_schedule_check_has_teeth():
+    # a ring too small for the server's three slots cannot be scheduled
+    with pytest.raises(AssertionError):
+        _ring_schedule(4, 2, False, False, ntiles=2)
+    # holding all three server slots to the end of the tile needs them free
+    # ahead of the next tile's first worker: fine with 4 slots, and the late
+    # release of two slots is what the LAMB three-CTA shape uses
+    assert _ring_schedule(4, 3, False, True, ntiles=3) == 3 * 6
+
+
+def test_late_server_reads_only_in_three_cta_lamb_shapes():
+    text = open(HDR).read()
+    assert "constexpr bool LATE = !ADAM && MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3;" in text
+    for nt, slots, nslot, c, gk, ndraw in SHAPES:
+        ring = nslot * nt * 4 * slots * 4
+        three = not ndraw and ring <= 72 * 1024
+        if three:
+            assert nslot >= 4, "the late server pass holds S, D and F in the ring at once"
