@@ -1114,8 +1114,11 @@ cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads&
     // BERT-Base 2.05 -> 1.99 ms).  With bfloat16 errors the wider CTA runs
     // 23 % slower, so those keep 256 threads, and at C = 4096 run three CTAs
     // per SM with a 4-slot ring (1-bit LAMB reading its server inputs late:
-    // BERT-Large fused kernel 8.55 -> 7.71 ms, same box).  In-kernel gradients
-    // at C = 4096 add 512 draw threads (draw_gradients).
+    // BERT-Large fused kernel 8.55 -> 7.71 ms, same box).  1-bit Adam with
+    // binary32 errors at C = 4096 takes the same three-CTA shape (10.79 ->
+    // 10.54 ms); 1-bit LAMB there spills at its 80 registers and keeps the
+    // 512-thread tile (11.06 against 11.22 ms).  In-kernel gradients at
+    // C = 4096 add 512 draw threads (draw_gradients).
     switch (P.C) {
     case 256:  return launch_grad<256, 4, 7, 256, ADAM, EB>(P, D, G, st);
     case 512:  return launch_grad<256, 4, 7, 512, ADAM, EB>(P, D, G, st);
@@ -1125,11 +1128,13 @@ cudaError_t launch_fused_all_chunks(const Problem& P, const Dev& D, const Grads&
             if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 2048, ADAM, EB>(P, D, G, st);
         return launch_grad<256, 4, 7, 2048, ADAM, EB>(P, D, G, st);
     case 4096:
-        if constexpr (!EB)
-            if (G.kind == kGradF32) return launch_one<512, 2, kGradF32, 7, 4096, ADAM, EB>(P, D, G, st);
         if (G.kind == kGradPhilox) return launch_one<512, 2, kGradPhilox, 7, 4096, ADAM, EB, 512>(P, D, G, st);
-        if constexpr (EB)           // three CTAs per SM with a 4-slot ring
-            if (G.kind == kGradF32) return launch_one<256, 4, kGradF32, 4, 4096, ADAM, EB>(P, D, G, st);
+        if (G.kind == kGradF32) {
+            if constexpr (ADAM || EB)   // three CTAs per SM with a 4-slot ring
+                return launch_one<256, 4, kGradF32, 4, 4096, ADAM, EB>(P, D, G, st);
+            else
+                return launch_one<512, 2, kGradF32, 7, 4096, ADAM, EB>(P, D, G, st);
+        }
         return launch_grad<256, 4, 7, 4096, ADAM, EB>(P, D, G, st);
     case 8192: return launch_grad<512, 4, 7, 8192, ADAM, EB>(P, D, G, st);
     default:   return cudaErrorInvalidValue;

@@ -35,12 +35,14 @@ PLANS = {
     "large": dict(n_warm=10, n_comp=100, checkpoints=(9, "freeze", 10, 19, 109)),
     "large_w32": dict(n_warm=50, n_comp=50, checkpoints=(48, 49, "freeze", 50, 51, 99)),
     "gpt2xl": dict(n_warm=10, n_comp=50, checkpoints=(9, "freeze", 10, 19, 59)),
-    # the options on the BERT-Large table: bfloat16 error storage with each
-    # method variant (variant 1 = 1-bit Adam)
+    # the options on the BERT-Large table, each with its own kernel shape:
+    # bfloat16 error storage with each method variant, and 1-bit Adam
+    # (variant 1)
     "large:adam+bf16err": dict(n_warm=10, n_comp=20, checkpoints=(9, "freeze", 10, 29),
                                variant=1, error_storage=1),
     "large:bf16err": dict(n_warm=10, n_comp=20, checkpoints=(9, "freeze", 10, 29),
                           error_storage=1),
+    "large:adam": dict(n_warm=10, n_comp=20, checkpoints=(9, "freeze", 10, 29), variant=1),
 }
 
 # sampled elements per workload (bounds the oracle's CPU time), and the

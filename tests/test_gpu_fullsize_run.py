@@ -2,9 +2,9 @@
 C=2048, 10 warmup + 10 compression steps), BERT-Large (W=16, C=4096, 10 +
 100), BERT-Large with 32 workers and in-kernel gradients (50 + 50: the
 warmup-to-compression switch at step 50) and GPT-2-XL with bfloat16
-gradients (W=8, C=8192, 10 + 50); and on the BERT-Large table the two
-options that select other kernel shapes, bfloat16 error storage with 1-bit
-LAMB and with 1-bit Adam (10 + 20 each).
+gradients (W=8, C=8192, 10 + 50); and on the BERT-Large table the
+options that select other kernel shapes: bfloat16 error storage with 1-bit
+LAMB and with 1-bit Adam, and 1-bit Adam (10 + 20 each).
 
 The GPU runs every step of the configuration from the seeded initial
 parameters, through the real variance freeze and the first compression
@@ -126,7 +126,7 @@ def _close_per_frag(a, b, frags, tol):
 
 
 @pytest.mark.parametrize("name", ["base", "large", "large_w32", "gpt2xl", "large:adam+bf16err",
-                                  "large:bf16err"])
+                                  "large:bf16err", "large:adam"])
 def test_full_size_whole_run(name):
     wl, tensors, runs = fullrun.plan(name)
     pl = fullrun.PLANS[name]
