@@ -540,12 +540,14 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     // but in that BERT-Large instantiation (3 % slower there), which keeps the
     // plain division and square root.
     constexpr bool FAST_SCALE = !(NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox);
-    // With three CTAs per SM (80 registers a thread), 1-bit LAMB's server
-    // pass reads the frozen preconditioner and the old fresh variance from
-    // the ring after its chunk-norm barrier instead of holding them in
-    // registers across it (which spilled), and releases those two slots at
-    // the end of the tile.
-    constexpr bool LATE = !ADAM && MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3;
+    // With three CTAs per SM (80 registers a thread) or with draw warps (64),
+    // 1-bit LAMB's server pass reads the frozen preconditioner and the old
+    // fresh variance from the ring after its chunk-norm barrier instead of
+    // holding them in registers across it (which spilled), and releases
+    // those two slots at the end of the tile (BERT-Large with bfloat16
+    // errors 8.55 -> 7.71 ms, W = 32 with in-kernel gradients 54.15 -> 52.96
+    // ms, same box).
+    constexpr bool LATE = !ADAM && (MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3 || NDRAW > 0);
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;

@@ -146,12 +146,13 @@ def test_shape_bounds(nt, slots, nslot, c, gk, ndraw):
             assert tile // 8 + sbytes <= slot_bytes
 
 
-def _ring_schedule(W, nslot, adam, late, ntiles):
+def _ring_schedule(W, nslot, adam, late, ntiles, per_worker=2):
     """The fused kernel's copy-ring schedule, restated: thread 0 issues items
     in order while their slots fit ahead of the released positions; the
     compressing threads wait for an item's slots, and release them after the
     barrier that follows their last read.  Items per tile: M (1 slot), W
-    workers (gradients + errors, 2 slots each), the server's S (errors, and
+    workers (gradients + errors, 2 slots each; errors only, 1 slot, when the
+    gradients are drawn in the kernel), the server's S (errors, and
     for 1-bit LAMB the frozen preconditioner: 1 or 2 slots) and, for 1-bit
     LAMB, F (old fresh variance, 1 slot).  With late server reads the
     preconditioner and F slots are released only at the end of the tile.
@@ -162,7 +163,7 @@ def _ring_schedule(W, nslot, adam, late, ntiles):
     n_items = W + (2 if adam else 3)
 
     def slots(r):
-        return 1 if r == 0 else (2 if r <= W else (kserver if r == W + 1 else 1))
+        return 1 if r == 0 else (per_worker if r <= W else (kserver if r == W + 1 else 1))
 
     st = dict(issue_pos=0, released=0, tile=0, r=0, cp=0, waits=0)
 
@@ -190,8 +191,8 @@ def _ring_schedule(W, nslot, adam, late, ntiles):
     for _ in range(ntiles):
         wait(1)                                         # M
         for w in range(W):
-            wait(2)
-            release(3 if w == 0 else 2)                 # after the worker's barrier
+            wait(per_worker)
+            release(1 + per_worker if w == 0 else per_worker)   # after the worker's barrier
         nsrv = kserver + (0 if adam else 1)
         wait(nsrv)
         release(1 if late else nsrv)                    # after the server's barrier
@@ -202,10 +203,11 @@ def _ring_schedule(W, nslot, adam, late, ntiles):
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 16, 32])
-@pytest.mark.parametrize("nslot,adam,late", [(7, False, False), (7, True, False), (4, True, False),
-                                             (4, False, True), (4, False, False)])
-def test_ring_schedule_never_waits_for_an_unissued_copy(W, nslot, adam, late):
-    assert _ring_schedule(W, nslot, adam, late, ntiles=5) == 5 * (W + 2)
+@pytest.mark.parametrize("nslot,adam,late,per_worker", [
+    (7, False, False, 2), (7, True, False, 2), (4, True, False, 2), (4, False, True, 2),
+    (4, False, False, 2), (7, False, True, 1), (7, True, False, 1)])
+def test_ring_schedule_never_waits_for_an_unissued_copy(W, nslot, adam, late, per_worker):
+    assert _ring_schedule(W, nslot, adam, late, ntiles=5, per_worker=per_worker) == 5 * (W + 2)
 
 
 def test_ring_schedule_check_has_teeth():
@@ -220,7 +222,7 @@ def test_ring_schedule_check_has_teeth():
 
 def test_late_server_reads_only_in_three_cta_lamb_shapes():
     text = open(HDR).read()
-    assert "constexpr bool LATE = !ADAM && MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3;" in text
+    assert "constexpr bool LATE = !ADAM && (MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3 || NDRAW > 0);" in text
     for nt, slots, nslot, c, gk, ndraw in SHAPES:
         ring = nslot * nt * 4 * slots * 4
         three = not ndraw and ring <= 72 * 1024
