@@ -137,11 +137,19 @@ def kernel_source_hash():
 ISSUE_PEAK = 152 * 4 * 32 * 2070e6    # thread instructions per second (SMs x schedulers x lanes x clock)
 
 
-def profiled_instructions(workload_name):
+def profile_summary(workload_name, variant="lamb", errors="f32"):
+    """Path, relative to the repository, of the committed ncu summary of the
+    fused kernel that this workload, method variant and error storage
+    launch (each combination is its own kernel instantiation)."""
+    tag = workload_name + ("_adam" if variant == "adam" else "") + ("_bf16err" if errors == "bf16" else "")
+    return os.path.join("profiles", f"compress_kernel_{tag}.md")
+
+
+def profiled_instructions(workload_name, variant="lamb", errors="f32"):
     """Thread instructions per launch of the fused kernel from the committed
     ncu summary (in-kernel gradient workloads), if taken on the current
     kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"compress_kernel_{workload_name}.md")
+    path = os.path.join(ROOT, profile_summary(workload_name, variant, errors))
     if not os.path.exists(path):
         return None
     m = re.search(r"thread_inst_per_launch:\s*([0-9.eE+]+)\s+source_sha:\s*([0-9a-f]+)", open(path).read())
@@ -150,14 +158,14 @@ def profiled_instructions(workload_name):
     return float(m.group(1))
 
 
-def profiled_traffic(workload_name):
+def profiled_traffic(workload_name, variant="lamb", errors="f32"):
     """dram bytes per launch of the fused kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None.
     Returns (bytes or None, a description of where the figure comes from).
     It is not measured in this run: a DRAM-counter capture of the full-size
     workload is not taken under the profiler (the summary scales a small
     capture of the same kernel by the parameters processed)."""
-    rel = os.path.join("profiles", f"compress_kernel_{workload_name}.md")
+    rel = profile_summary(workload_name, variant, errors)
     path = os.path.join(ROOT, rel)
     if not os.path.exists(path):
         return None, f"no ncu summary {rel}"
@@ -485,7 +493,7 @@ def run_ours(args, world, rank, local):
     kb = fused_kernel_bytes(wl, args.variant, args.errors)
     k_avg = statistics.mean(kern_ms)
     achieved = kb / (k_avg / 1e3) / 1e9
-    traffic, traffic_source = profiled_traffic(wl.name)
+    traffic, traffic_source = profiled_traffic(wl.name, args.variant, args.errors)
     copy_now = live_copy_gbs()
     roofline = {"bound": "hbm", "kernel": "k_compress (fused worker+server pass)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -495,7 +503,7 @@ def run_ours(args, world, rank, local):
                 "live_copy_gbs": copy_now, "frac_of_live_copy": achieved / copy_now}
     if wl.grad == "philox":
         # gradients drawn in the kernel: bound by instruction issue, not HBM
-        inst = profiled_instructions(wl.name)
+        inst = profiled_instructions(wl.name, args.variant, args.errors)
         if inst is not None:
             t_ips = inst / (k_avg / 1e3)
             roofline = {"bound": "alu", "kernel": "k_compress (fused, in-kernel gradients)",
