@@ -530,12 +530,12 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     constexpr int GKC = DRAW ? kGradF32 : GK;   // how the compressing threads read gradients
     // Full tiles do their element-wise sums in packed pairs (f32x2.cuh; the
     // same bits as the scalar form) where that measured faster: BERT-Base
-    // (512 x 2, C = 2048), bfloat16 errors, C = 8192, and 1-bit Adam with
-    // in-kernel gradients.  The 512 x 2 tiles at C = 4096 otherwise keep the
-    // scalar form: with stored gradients (BERT-Large) the packed sums ran 2 %
-    // slower (the server pass alone spilled at 64 registers), and 1-bit LAMB
-    // with draw warps spills less without them (54.6 against 56.3 ms).
-    constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096) || (GK == kGradPhilox && ADAM);
+    // (512 x 2, C = 2048), bfloat16 errors, C = 8192, and in-kernel
+    // gradients (1-bit LAMB with its late server reads: 52.90 -> 52.34 ms).
+    // The 512 x 2 tile with stored gradients at C = 4096 (BERT-Large) keeps
+    // the scalar form: the packed sums ran 2 % slower there (the server pass
+    // alone spilled at 64 registers).
+    constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096) || GK == kGradPhilox;
     // The chunk scale's shortcut (chunk_scale) measured faster everywhere
     // but in that BERT-Large instantiation (3 % slower there), which keeps the
     // plain division and square root.
