@@ -528,26 +528,28 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     // in-kernel gradients drawn by dedicated warps (see draw_gradients)
     constexpr bool DRAW = GK == kGradPhilox && NDRAW > 0;
     constexpr int GKC = DRAW ? kGradF32 : GK;   // how the compressing threads read gradients
+    // The 512 x 2 tile with stored gradients at C = 4096 (BERT-Large) is the
+    // one instantiation where the options below measured slower.
+    constexpr bool WIDE4096 = NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox;
     // Full tiles do their element-wise sums in packed pairs (f32x2.cuh; the
-    // same bits as the scalar form) where that measured faster: BERT-Base
-    // (512 x 2, C = 2048), bfloat16 errors, C = 8192, and in-kernel
-    // gradients (1-bit LAMB with its late server reads: 52.90 -> 52.34 ms).
-    // The 512 x 2 tile with stored gradients at C = 4096 (BERT-Large) keeps
-    // the scalar form: the packed sums ran 2 % slower there (the server pass
-    // alone spilled at 64 registers).
-    constexpr bool PACK = !(NT == 512 && SLOTS == 2 && C == 4096) || GK == kGradPhilox;
+    // same bits as the scalar form): faster for BERT-Base (512 x 2, C =
+    // 2048), bfloat16 errors, C = 8192 and in-kernel gradients (W = 32, 1-bit
+    // LAMB: 52.90 -> 52.34 ms); 2 to 5 % slower for WIDE4096, with or
+    // without spills.
+    constexpr bool PACK = !WIDE4096;
     // The chunk scale's shortcut (chunk_scale) measured faster everywhere
-    // but in that BERT-Large instantiation (3 % slower there), which keeps the
-    // plain division and square root.
-    constexpr bool FAST_SCALE = !(NT == 512 && SLOTS == 2 && C == 4096 && GK != kGradPhilox);
-    // With three CTAs per SM (80 registers a thread) or with draw warps (64),
+    // but in WIDE4096 (3 % slower there), which keeps the plain division and
+    // square root.
+    constexpr bool FAST_SCALE = !WIDE4096;
     // 1-bit LAMB's server pass reads the frozen preconditioner and the old
     // fresh variance from the ring after its chunk-norm barrier instead of
-    // holding them in registers across it (which spilled), and releases
-    // those two slots at the end of the tile (BERT-Large with bfloat16
-    // errors 8.55 -> 7.71 ms, W = 32 with in-kernel gradients 54.15 -> 52.96
-    // ms, same box).
-    constexpr bool LATE = !ADAM && (MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3 || NDRAW > 0);
+    // holding them in registers across it, and releases those two slots at
+    // the end of the tile.  It removes spills where registers are scarce
+    // (three CTAs per SM at 80 registers, draw warps at 64) and measured
+    // faster everywhere it was tried (same box, fused kernel: BERT-Large with
+    // bfloat16 errors 8.55 -> 7.71 ms, W = 32 with in-kernel gradients 54.15
+    // -> 52.96 ms, BERT-Base 1.937 -> 1.917 ms, GPT-2-XL 24.01 -> 23.61 ms).
+    constexpr bool LATE = !ADAM && !WIDE4096;
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");
     using R = Ring<TILE>;

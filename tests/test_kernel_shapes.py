@@ -220,11 +220,13 @@ def test_ring_schedule_check_has_teeth():
     assert _ring_schedule(4, 3, False, True, ntiles=3) == 3 * 6
 
 
-def test_late_server_reads_only_in_three_cta_lamb_shapes():
+def test_late_server_reads_fit_the_ring():
     text = open(HDR).read()
-    assert "constexpr bool LATE = !ADAM && (MinBlocks<NT, SLOTS, NSLOT, NDRAW>::value >= 3 || NDRAW > 0);" in text
+    assert "constexpr bool LATE = !ADAM && !WIDE4096;" in text
     for nt, slots, nslot, c, gk, ndraw in SHAPES:
-        ring = nslot * nt * 4 * slots * 4
-        three = not ndraw and ring <= 72 * 1024
-        if three:
-            assert nslot >= 4, "the late server pass holds S, D and F in the ring at once"
+        # the server holds S, D and F (three slots) until the end of the tile,
+        # and the next tile's momentum slot must fit beside them
+        assert nslot >= 4
+        per_worker = 1 if gk == 2 else 2
+        for W in (1, 2, 16, 33):
+            _ring_schedule(W, nslot, False, True, ntiles=3, per_worker=per_worker)
