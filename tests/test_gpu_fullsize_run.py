@@ -125,11 +125,10 @@ def _close_per_frag(a, b, frags, tol):
     return True, None
 
 
-@pytest.mark.parametrize("name", ["base", "large", "large_w32", "gpt2xl", "large:adam+bf16err",
-                                  "large:bf16err", "large:adam"])
-def test_full_size_whole_run(name):
-    wl, tensors, runs = fullrun.plan(name)
-    pl = fullrun.PLANS[name]
+def run_and_compare(name, wl, runs, pl):
+    """The plan's whole run on the GPU and, in spawned processes at the same
+    time, the oracle's runs; then every compared value, run by run.  Returns
+    the number of tensors covered completely."""
     N, W, C = wl.N, wl.W, wl.chunk
     gc.collect()
     torch.cuda.empty_cache()              # earlier full-size tests' cached blocks
@@ -193,5 +192,13 @@ def test_full_size_whole_run(name):
         e0 += n
         w0 += nw
         k0c += nk
-    assert covered >= 100 or name == "large_w32" and covered >= 50, covered
     assert diffs == 0, f"{diffs} compared floats differ in some bit"
+    return covered
+
+
+@pytest.mark.parametrize("name", ["base", "large", "large_w32", "gpt2xl", "large:adam+bf16err",
+                                  "large:bf16err", "large:adam"])
+def test_full_size_whole_run(name):
+    wl, tensors, runs = fullrun.plan(name)
+    covered = run_and_compare(name, wl, runs, fullrun.PLANS[name])
+    assert covered >= 100 or name == "large_w32" and covered >= 50, covered
