@@ -15,7 +15,7 @@ sign words bit-exact, every other value bit-identical."""
 import pytest
 
 import workload
-from test_gpu_fullsize_run import run_and_compare
+from fullrun_gpu import run_and_compare
 
 pytestmark = pytest.mark.gpu
 
