@@ -163,8 +163,19 @@ def test_bf16_error_storage(variant):
 @pytest.mark.parametrize("variant", [0, 1])
 def test_bf16_error_storage_4096(variant):
     """bfloat16 errors with 4096-element chunks and W = 16 (the BERT-Large
-    shape of that option; 1-bit Adam runs it at three CTAs per SM)."""
+    shape of that option: three CTAs per SM, a 4-slot ring, and for 1-bit
+    LAMB the server's late reads)."""
     run(bert_mini(W=16, chunk=4096), 4, 6, variant=variant, error_storage=1)
+
+
+@pytest.mark.parametrize("W", [1, 2, 37])
+@pytest.mark.parametrize("variant,errors", [(0, 1), (1, 0), (1, 1)])
+def test_three_cta_shape_worker_counts(W, variant, errors):
+    """The three-CTA, 4-slot shape (C = 4096 with bfloat16 errors or 1-bit
+    Adam) with one, two and an odd number of workers: the copy ring's
+    schedule changes with W (one worker item of two slots, or many), and
+    the late server reads keep two slots to the end of every tile."""
+    run(bert_mini(W=W, chunk=4096), 2, 3, variant=variant, error_storage=errors)
 
 
 def test_bf16_error_storage_with_bf16_and_in_kernel_gradients():
