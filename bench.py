@@ -126,11 +126,50 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_tokens(text):
+    """C/C++ source with its comments removed and every run of whitespace
+    outside string and character literals collapsed to one space: two
+    sources that differ only in comments or layout give the same text."""
+    out, i, n = [], 0, len(text)
+    space = False
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            space = True
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            space = True
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            if space and out:
+                out.append(" ")
+            space = False
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif c.isspace():
+            space = True
+            i += 1
+        else:
+            if space and out:
+                out.append(" ")
+            space = False
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash():
+    """Hash of the fused kernel's code (comments and layout ignored), so an
+    ncu summary stays attached to the code it measured."""
     h = hashlib.sha1()
     for f in ("k_compress.cuh", "k_compress.cu", "lamb1b_internal.cuh", "philox.cuh", "f32x2.cuh"):
-        with open(os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "communication_compressed_optimizer_gb300", "csrc", f)) as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()[:12]
 
 

@@ -546,9 +546,10 @@ __global__ void __launch_bounds__(NT + NDRAW, (MinBlocks<NT, SLOTS, NSLOT, NDRAW
     // holding them in registers across it, and releases those two slots at
     // the end of the tile.  It removes spills where registers are scarce
     // (three CTAs per SM at 80 registers, draw warps at 64) and measured
-    // faster everywhere it was tried (same box, fused kernel: BERT-Large with
-    // bfloat16 errors 8.55 -> 7.71 ms, W = 32 with in-kernel gradients 54.15
-    // -> 52.96 ms, BERT-Base 1.937 -> 1.917 ms, GPT-2-XL 24.01 -> 23.61 ms).
+    // faster in every shape that uses it (same box, fused kernel: BERT-Large
+    // with bfloat16 errors 8.55 -> 7.71 ms, W = 32 with in-kernel gradients
+    // 54.15 -> 52.96 ms, BERT-Base 1.937 -> 1.917 ms, GPT-2-XL 24.01 -> 23.61
+    // ms); in WIDE4096 it ran slower (11.11 against 10.92 ms).
     constexpr bool LATE = !ADAM && !WIDE4096;
     static_assert(NDRAW == 0 || GK == kGradPhilox, "draw warps only for in-kernel gradients");
     static_assert(TILE % C == 0, "a tile holds whole chunks");

@@ -26,3 +26,13 @@ def test_committed_summaries_name_a_kernel_source():
         if f.startswith("compress_kernel_"):
             text = open(os.path.join(root, "profiles", f)).read()
             assert "source_sha:" in text, f
+
+
+def test_code_hash_ignores_comments_and_layout_only():
+    a = 'int f(int x) {  // one\n  return x + 1; /* two */ }\nconst char* s = "a // b";\n'
+    b = 'int f(int x) { return x + 1; }\n/* moved */ const char* s = "a // b";'
+    assert bench.code_tokens(a) == bench.code_tokens(b)
+    assert bench.code_tokens('s = "a // b";') == 's = "a // b";'       # literals are kept whole
+    assert bench.code_tokens("c = '/'; d = a / b;") == "c = '/'; d = a / b;"
+    assert bench.code_tokens(a) != bench.code_tokens(a.replace("x + 1", "x + 2"))
+    assert bench.code_tokens(a) != bench.code_tokens(a.replace('"a // b"', '"a  // b"'))
