@@ -130,7 +130,10 @@ struct GradBytes { static constexpr int value = GK == kGradF32 ? 4 : (GK == kGra
 // server message), then per worker W_w its gradients (when stored) and its
 // error, then S (e_s, and for 1-bit LAMB the frozen sqrt(v) + eps), then F
 // (v_fresh, 1-bit LAMB only).  Slot position p lives in slot p % NSLOT
-// and completes phase (p / NSLOT) of that slot's barrier.
+// and completes phase (p / NSLOT) of that slot's barrier.  Positions are
+// released in order, at the barrier after their last read: a worker's at
+// its chunk-norm barrier, S's at the server's, and with late server reads
+// (LATE) the frozen preconditioner's and F's at the end of the tile.
 template <int TILE>
 struct Ring {
     static constexpr uint32_t kSlot = TILE * 4;
