@@ -83,6 +83,22 @@ MUTATIONS = [
      "u[i] = fadd(fdiv(s->m[i], d), fmul(s->wd, s->x[i]));", "u[i] = fdiv(s->m[i], d);"),
     ("a NaN ratio ignored by the per-tensor maximum",
      "if (rho) rho[j] = (r != r) ? INFINITY : r;", "if (rho) rho[j] = r;"),
+    ("worker momentum with beta1 and 1-beta1 swapped",
+     "float mw = fadd(fmul(s->beta1, s->m[i]), fmul(w1, g[(int64_t)w * ld + i]));",
+     "float mw = fadd(fmul(w1, s->m[i]), fmul(s->beta1, g[(int64_t)w * ld + i]));"),
+    ("warmup momentum with beta1 and 1-beta1 swapped",
+     "s->m[i] = fadd(fmul(s->beta1, s->m[i]), fmul(w1, gb));",
+     "s->m[i] = fadd(fmul(w1, s->m[i]), fmul(s->beta1, gb));"),
+    ("eps inside the square root of the warmup direction",
+     "float d = fadd(fsqrt(s->v[i]), s->eps);\n        u[i] =",
+     "float d = fsqrt(fadd(s->v[i], s->eps));\n        u[i] ="),
+    ("trust ratio not clipped",
+     "float c = clip(ratio, s->cmin, s->cmax);", "float c = ratio;"),
+    ("compression-stage ratio not clipped to its factor bounds",
+     "float r = clip(R, fmin, fmax);", "float r = R;"),
+    ("scatter keeps each worker's own momentum (server result dropped)",
+     "if (rho) rho[j] = (r != r) ? INFINITY : r;\n        s->m[i] = m_new;",
+     "if (rho) rho[j] = (r != r) ? INFINITY : r;"),
     ("1-bit Adam tracks a fresh variance",
      "        if (s->variant == 1) {      /* 1-bit Adam: no fresh variance, no ratio */",
      "        if (s->variant == 99) {      /* 1-bit Adam: no fresh variance, no ratio */"),
