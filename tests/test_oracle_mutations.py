@@ -65,6 +65,8 @@ MUTATIONS = [
      "s->v[i] = fadd(fmul(s->beta2, s->v[i]), fmul(w2, fmul(s->m[i], s->m[i])));"),
     ("sign of zero sent as -1",
      "int pos = !(z[j] < 0.0f);", "int pos = (z[j] > 0.0f);"),
+    ("sign of NaN sent as -1 (zeros still +1)",
+     "int pos = !(z[j] < 0.0f);", "int pos = (z[j] >= 0.0f);"),
     ("sign bits packed MSB first",
      "if (pos) words[j / 32] |= 1u << (j % 32);", "if (pos) words[j / 32] |= 1u << (31 - j % 32);"),
     ("1-bit Adam compression stage scaled by c_bar",
@@ -99,6 +101,16 @@ MUTATIONS = [
     ("scatter keeps each worker's own momentum (server result dropped)",
      "if (rho) rho[j] = (r != r) ? INFINITY : r;\n        s->m[i] = m_new;",
      "if (rho) rho[j] = (r != r) ? INFINITY : r;"),
+    ("ratio taken from the fresh variance before this step's update",
+     "s->v_fresh[i] = fadd(fmul(s->beta2, s->v_fresh[i]), fmul(w2, fmul(gt, gt)));\n"
+     "        float num = fadd(fsqrt(s->v[i]), s->eps);\n"
+     "        float den = fadd(fsqrt(s->v_fresh[i]), s->eps);",
+     "float num = fadd(fsqrt(s->v[i]), s->eps);\n"
+     "        float den = fadd(fsqrt(s->v_fresh[i]), s->eps);\n"
+     "        s->v_fresh[i] = fadd(fmul(s->beta2, s->v_fresh[i]), fmul(w2, fmul(gt, gt)));"),
+    ("compression-stage update without the learning rate",
+     "float gc = fmul(s->lr, c);\n    for (int64_t i = lo; i < hi; ++i) {",
+     "float gc = c;\n    for (int64_t i = lo; i < hi; ++i) {"),
     ("1-bit Adam tracks a fresh variance",
      "        if (s->variant == 1) {      /* 1-bit Adam: no fresh variance, no ratio */",
      "        if (s->variant == 99) {      /* 1-bit Adam: no fresh variance, no ratio */"),
