@@ -129,7 +129,9 @@ def measured_peaks():
 def code_tokens(text):
     """C/C++ source with its comments removed and every run of whitespace
     outside string and character literals collapsed to one space: two
-    sources that differ only in comments or layout give the same text."""
+    sources that differ only in comments or layout give the same text.
+    (Raw string literals and digit separators are not recognised; the kernel
+    sources use neither.)"""
     out, i, n = [], 0, len(text)
     space = False
     while i < n:
