@@ -110,15 +110,18 @@ def test_adam_variant_in_kernel_gradients():
 
 # ---- non-finite inputs ---------------------------------------------------------
 
-def test_nonfinite_gradients_propagate_like_the_oracle():
+@pytest.mark.parametrize("error_storage", [0, 1])
+def test_nonfinite_gradients_propagate_like_the_oracle(error_storage):
     """A NaN and an Inf gradient in one worker's chunk: NaN sends +1 (sign
     bit rule), the chunk's scale and errors become NaN, the server chunk
     follows, the tensor's ratio max counts NaN as +Inf; every word and every
-    NaN position agrees with the oracle."""
+    NaN position agrees with the oracle.  With bfloat16 error storage the
+    stored error bits themselves, NaNs included (0x7FC0), equal the
+    oracle's."""
     import numpy as np
     import torch
     wl = bert_mini(W=4, chunk=1024)
-    p = Pair(wl)
+    p = Pair(wl, error_storage=error_storage)
     for _ in range(2):
         p.warmup()
     p.freeze()
@@ -140,6 +143,12 @@ def test_nonfinite_gradients_propagate_like_the_oracle():
         fin = ~np.isnan(getattr(o, k))
         np.testing.assert_array_equal(st[k][:wl.N][fin], getattr(o, k)[fin], err_msg=k)
     np.testing.assert_array_equal(np.isnan(st["e_w"][:, :wl.N]), np.isnan(o.e_w))
+    if error_storage:
+        for k in ("e_w", "e_s"):
+            got = np.ascontiguousarray(st[k][..., :wl.N]).view(np.uint32)
+            want = np.ascontiguousarray(getattr(o, k)).view(np.uint32)
+            assert np.isnan(getattr(o, k)).any(), k
+            np.testing.assert_array_equal(got, want, err_msg=k)
     np.testing.assert_array_equal(np.isnan(st["scale_w"]), np.isnan(o.scale_w))
     np.testing.assert_array_equal(np.isnan(st["x"]), np.isnan(o.x))
     fin = ~np.isnan(o.x)
