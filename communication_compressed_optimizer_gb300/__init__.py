@@ -137,6 +137,7 @@ class OneBitLamb:
             ctypes.c_void_p(params.data_ptr()), ctypes.c_void_p(self.workspace.data_ptr()),
             int(nbytes), _stream_handle(stream)))
         self.N = params.numel()
+        self.K = -(-self.N // self.chunk)
 
     # -- steps -------------------------------------------------------------
     def warmup_step(self, grads, stream=None):
@@ -152,6 +153,42 @@ class OneBitLamb:
         d = _grads_desc(grads, self.N)
         _abi.check("lamb1b_compress_step",
                    self._lib.lamb1b_compress_step(self._ctx, ctypes.byref(d), _stream_handle(stream)))
+
+    def compress_step_host(self, host_grads, staging, words_out=None, scales_out=None, stream=None,
+                           copy_stream=None):
+        """One compression step whose gradients are in pinned host memory.
+
+        host_grads: a pinned CPU tensor [W, ld] (float32, or bfloat16 bits as
+        bfloat16/int16); staging: a CUDA tensor of the same shape, strides and
+        dtype that receives them; words_out / scales_out: None or pinned CPU
+        tensors of ceil(N/32) int32 and K float32 that receive the step's
+        server message.  The copy runs on copy_stream (default: the step's
+        stream); with two staging tensors used in turn and a separate
+        copy_stream, a step's copy overlaps the previous step's kernels."""
+        torch = _torch()
+        if (not isinstance(host_grads, torch.Tensor) or host_grads.is_cuda
+                or not host_grads.is_pinned()):
+            raise TypeError("host_grads: a pinned CPU tensor [W, ld]")
+        if (not isinstance(staging, torch.Tensor) or not staging.is_cuda
+                or staging.shape != host_grads.shape or staging.stride() != host_grads.stride()
+                or staging.dtype != host_grads.dtype):
+            raise ValueError("staging: a CUDA tensor with host_grads' shape, strides and dtype")
+        d = _grads_desc(staging, self.N)
+        d.ptr = host_grads.data_ptr()
+        outs = []
+        for t, n, dt in ((words_out, -(-self.N // 32), (torch.int32, torch.uint32)),
+                         (scales_out, self.K, (torch.float32,))):
+            if t is None:
+                outs.append(None)
+                continue
+            if t.is_cuda or not t.is_pinned() or t.dtype not in dt or t.numel() < n or not t.is_contiguous():
+                raise ValueError("words_out / scales_out: pinned contiguous CPU tensors of the message's size")
+            outs.append(ctypes.c_void_p(t.data_ptr()))
+        _abi.check("lamb1b_compress_step_host",
+                   self._lib.lamb1b_compress_step_host(
+                       self._ctx, ctypes.byref(d), ctypes.c_void_p(staging.data_ptr()), outs[0], outs[1],
+                       _stream_handle(stream),
+                       _stream_handle(copy_stream if copy_stream is not None else stream)))
 
     def check_status(self, stream=None):
         _abi.check("lamb1b_check_status",

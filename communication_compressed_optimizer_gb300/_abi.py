@@ -18,7 +18,8 @@ ERR_ARG, ERR_ALIGN, ERR_WORKSPACE, ERR_STATE, ERR_CUDA, ERR_NONFINITE, ERR_DEVIC
 GRAD_F32, GRAD_BF16, GRAD_PHILOX = 0, 1, 2
 
 EXPORTED = ("lamb1b_workspace_bytes", "lamb1b_init", "lamb1b_warmup_step",
-            "lamb1b_freeze_variance", "lamb1b_compress_step", "lamb1b_state_view",
+            "lamb1b_freeze_variance", "lamb1b_compress_step", "lamb1b_compress_step_host",
+            "lamb1b_state_view",
             "lamb1b_set_counters", "lamb1b_check_status", "lamb1b_set_trace_events",
             "lamb1b_set_fault_injection", "lamb1b_sync_momentum", "lamb1b_destroy",
             "lamb1b_error_string", "lamb1b_gen_grads", "lamb1b_gen_params",
@@ -85,6 +86,7 @@ def load(build_if_missing: bool = False):
     L.lamb1b_warmup_step.argtypes = [_P, ctypes.POINTER(GradsDesc), _P]
     L.lamb1b_freeze_variance.argtypes = [_P, _P]
     L.lamb1b_compress_step.argtypes = [_P, ctypes.POINTER(GradsDesc), _P]
+    L.lamb1b_compress_step_host.argtypes = [_P, ctypes.POINTER(GradsDesc), _P, _P, _P, _P, _P]
     L.lamb1b_state_view.argtypes = [_P, ctypes.POINTER(State)]
     L.lamb1b_set_counters.argtypes = [_P, i64, i32, i32]
     L.lamb1b_check_status.argtypes = [_P, _P]

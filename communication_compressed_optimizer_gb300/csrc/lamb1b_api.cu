@@ -136,6 +136,28 @@ struct lamb1b_ctx {
     bool tracing = false;
     bool d_frz_valid = false;   // D.d_frz holds sqrt(v) + eps of the frozen v
     cudaEvent_t ev[4] = {};
+    // lamb1b_compress_step_host: the staging buffers seen lately, each with
+    // an event recorded after the last step that read it, so that the next
+    // copy into it waits for that step only
+    struct Staging {
+        const void* ptr = nullptr;
+        cudaEvent_t used = nullptr;
+        bool recorded = false;
+        uint64_t last = 0;
+    };
+    static constexpr int kStaging = 4;
+    Staging stg[kStaging];
+    uint64_t stg_clock = 0;
+    cudaEvent_t copied = nullptr;   // the host-to-device copy of a step is done
+    cudaEvent_t fence = nullptr;    // all work enqueued on the step stream so far
+
+    ~lamb1b_ctx()
+    {
+        for (Staging& e : stg)
+            if (e.used) cudaEventDestroy(e.used);
+        if (copied) cudaEventDestroy(copied);
+        if (fence) cudaEventDestroy(fence);
+    }
 };
 
 namespace {
@@ -358,6 +380,59 @@ extern "C" int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream)
     return LAMB1B_OK;
 }
 
+namespace {
+
+// The kernels of one compression step on checked gradients.
+int compress_enqueue(lamb1b_ctx* ctx, const lamb1b_grads* grads, cudaStream_t st)
+{
+    const Grads G = to_grads(ctx, grads);
+    // after the first compression step m lives in the server's sign words
+    // and chunk scales; before it, in the dense buffer the warmup left
+    ctx->P.m_packed = ctx->t > ctx->n_warm ? 1 : 0;
+    if (!ctx->d_frz_valid) {     // after a restore: rebuild sqrt(v) + eps of the frozen v
+        if (lamb1b::launch_frozen_denominator(ctx->P, ctx->D, st) != cudaSuccess) return LAMB1B_ERR_CUDA;
+        ctx->d_frz_valid = true;
+    }
+    if (lamb1b::launch_compress(ctx->P, ctx->D, G, ctx->x, st, ctx->tracing ? ctx->ev : nullptr) !=
+        cudaSuccess)
+        return LAMB1B_ERR_CUDA;
+    ctx->t += 1;
+    return LAMB1B_OK;
+}
+
+bool is_pinned_host_ptr(const void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+int refuse_capture(cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return LAMB1B_ERR_CUDA;
+    }
+    return cs == cudaStreamCaptureStatusNone ? LAMB1B_OK : LAMB1B_ERR_ARG;
+}
+
+int make_event(cudaEvent_t* e)
+{
+    if (*e) return LAMB1B_OK;
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        *e = nullptr;
+        return LAMB1B_ERR_CUDA;
+    }
+    return LAMB1B_OK;
+}
+
+}  // namespace
+
 extern "C" int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, void* stream)
 {
     if (!ctx) return LAMB1B_ERR_ARG;
@@ -365,21 +440,75 @@ extern "C" int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, 
     int rc = device_check(ctx);
     if (rc) return rc;
     if ((rc = grads_check(ctx, grads))) return rc;
-    const Grads G = to_grads(ctx, grads);
-    // after the first compression step m lives in the server's sign words
-    // and chunk scales; before it, in the dense buffer the warmup left
-    ctx->P.m_packed = ctx->t > ctx->n_warm ? 1 : 0;
     NvtxRange range("lamb1b compression step");
-    if (!ctx->d_frz_valid) {     // after a restore: rebuild sqrt(v) + eps of the frozen v
-        if (lamb1b::launch_frozen_denominator(ctx->P, ctx->D, static_cast<cudaStream_t>(stream)) !=
-            cudaSuccess)
-            return LAMB1B_ERR_CUDA;
-        ctx->d_frz_valid = true;
+    return compress_enqueue(ctx, grads, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lamb1b_compress_step_host(lamb1b_ctx* ctx, const lamb1b_grads* host_grads, void* staging,
+                                         uint32_t* words_host, float* scales_host, void* stream,
+                                         void* copy_stream)
+{
+    if (!ctx || !host_grads) return LAMB1B_ERR_ARG;
+    if (ctx->stage != 1) return LAMB1B_ERR_STATE;
+    int rc = device_check(ctx);
+    if (rc) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t cst = static_cast<cudaStream_t>(copy_stream);
+    // first, so that no pointer query runs inside a capture
+    if ((rc = refuse_capture(st)) || (rc = refuse_capture(cst))) return rc;
+    if (host_grads->kind != LAMB1B_GRAD_F32 && host_grads->kind != LAMB1B_GRAD_BF16) return LAMB1B_ERR_ARG;
+    if (!host_grads->ptr || !is_pinned_host_ptr(host_grads->ptr)) return LAMB1B_ERR_ARG;
+    if ((words_host && !is_pinned_host_ptr(words_host)) || (scales_host && !is_pinned_host_ptr(scales_host)))
+        return LAMB1B_ERR_ARG;
+    lamb1b_grads dev = *host_grads;      // the same rows, in the staging buffer
+    dev.ptr = staging;
+    if ((rc = grads_check(ctx, &dev))) return rc;
+    if ((rc = make_event(&ctx->copied)) || (rc = make_event(&ctx->fence))) return rc;
+
+    // the staging buffer's entry: the last step that read it, or (a buffer
+    // not seen lately) everything enqueued on the step stream so far
+    lamb1b_ctx::Staging* e = nullptr;
+    for (lamb1b_ctx::Staging& s : ctx->stg)
+        if (s.ptr == staging) e = &s;
+    bool known = e != nullptr;
+    if (!known) {
+        e = &ctx->stg[0];
+        for (lamb1b_ctx::Staging& s : ctx->stg)
+            if (s.last < e->last) e = &s;
+        e->ptr = staging;
+        e->recorded = false;
     }
-    if (lamb1b::launch_compress(ctx->P, ctx->D, G, ctx->x, static_cast<cudaStream_t>(stream),
-                                ctx->tracing ? ctx->ev : nullptr) != cudaSuccess)
+    if ((rc = make_event(&e->used))) return rc;
+    e->last = ++ctx->stg_clock;
+
+    NvtxRange range("lamb1b compression step from host gradients");
+    const int64_t es = host_grads->kind == LAMB1B_GRAD_F32 ? 4 : 2;
+    const size_t bytes = (size_t)ctx->P.W * (size_t)host_grads->ld * (size_t)es;
+    bool ok = true;
+    if (known && e->recorded) {
+        ok = cudaStreamWaitEvent(cst, e->used, 0) == cudaSuccess;
+    } else {
+        ok = cudaEventRecord(ctx->fence, st) == cudaSuccess && cudaStreamWaitEvent(cst, ctx->fence, 0) == cudaSuccess;
+    }
+    ok = ok && cudaMemcpyAsync(staging, host_grads->ptr, bytes, cudaMemcpyHostToDevice, cst) == cudaSuccess &&
+         cudaEventRecord(ctx->copied, cst) == cudaSuccess && cudaStreamWaitEvent(st, ctx->copied, 0) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
         return LAMB1B_ERR_CUDA;
-    ctx->t += 1;
+    }
+    if ((rc = compress_enqueue(ctx, &dev, st))) return rc;
+    ok = cudaEventRecord(e->used, st) == cudaSuccess;
+    e->recorded = ok;
+    const int64_t nw = (ctx->P.N + 31) / 32;
+    if (ok && words_host)
+        ok = cudaMemcpyAsync(words_host, ctx->D.signs_s, (size_t)nw * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+    if (ok && scales_host)
+        ok = cudaMemcpyAsync(scales_host, ctx->D.scale_s, (size_t)ctx->P.K * 4, cudaMemcpyDeviceToHost, st) ==
+             cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return LAMB1B_ERR_CUDA;
+    }
     return LAMB1B_OK;
 }
 

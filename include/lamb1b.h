@@ -239,6 +239,37 @@ int lamb1b_freeze_variance(lamb1b_ctx* ctx, void* stream);
  * counter advances on direct calls.  Errors: STATE before the freeze. */
 int lamb1b_compress_step(lamb1b_ctx* ctx, const lamb1b_grads* grads, void* stream);
 
+/* The same compression step with its gradients in host memory, for callers
+ * whose gradients arrive on the host: the step copies them to the GPU, runs,
+ * and reads the server's message back.
+ *   host_grads   kind LAMB1B_GRAD_F32 or LAMB1B_GRAD_BF16; ptr = W rows of
+ *                ld elements in pinned (page-locked) host memory, the layout
+ *                lamb1b_compress_step takes on the device.
+ *   staging      a caller-owned device buffer of W x ld elements of the same
+ *                type on the context's GPU (16-byte aligned, ld x element
+ *                size a multiple of 16 bytes): the copy's destination.
+ *   words_host   pinned host memory for the step's server sign words,
+ *                ceil(N/32) uint32 (the signs_s of lamb1b_state_view), or NULL.
+ *   scales_host  pinned host memory for its K chunk scales (scale_s), or NULL.
+ *   stream       the stream of the step's kernels and of the read-back.
+ *   copy_stream  the stream of the host-to-device copy (may be `stream`).
+ * Order: the copy runs on copy_stream after the work already enqueued there
+ * and after the last step of this context that read `staging` (the context
+ * remembers the last 4 staging buffers; for any other buffer the copy waits
+ * for all work enqueued on `stream` so far, so pass the same `stream` to
+ * every step of a context); the kernels wait for the copy; the read-back
+ * follows the kernels on `stream`.  So with two staging buffers used in turn
+ * and a separate copy_stream, a step's copy overlaps the previous step's
+ * kernels.  The host buffers must stay valid and unchanged until `stream`
+ * has passed the step.  Not for stream capture: on a capturing stream it
+ * returns LAMB1B_ERR_ARG and enqueues nothing.
+ * Errors: STATE before the freeze; ARG (other gradient kinds, pageable or
+ * device memory where pinned host memory is required, staging not memory of
+ * the context's GPU, ld < N, a capturing stream); ALIGN; CUDA. */
+int lamb1b_compress_step_host(lamb1b_ctx* ctx, const lamb1b_grads* host_grads, void* staging,
+                              uint32_t* words_host, float* scales_host, void* stream,
+                              void* copy_stream);
+
 /* Fills *out with device pointers into the workspace and the counters. */
 int lamb1b_state_view(const lamb1b_ctx* ctx, lamb1b_state* out);
 
