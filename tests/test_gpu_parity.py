@@ -93,6 +93,22 @@ def test_odd_worker_count_and_large_w():
     run(bert_mini(W=37, chunk=512), 1, 2)
 
 
+def _small_table():
+    return workload.bert_tensors(1, 32, 128, 300, max_pos=64) + [("tail", (37,))]
+
+
+@pytest.mark.parametrize("W,chunk,grad,errors", [(256, 4096, "f32", 0), (255, 4096, "f32", 1),
+                                                 (256, 1024, "bf16", 0), (255, 4096, "philox", 0)])
+def test_maximum_worker_count(W, chunk, grad, errors):
+    """The largest worker counts the C ABI accepts (256, and 255, which is
+    not a power of two: the server average is a true division), in the
+    stored-gradient, bfloat16-error three-CTA and in-kernel-gradient
+    shapes."""
+    kw = dict(heavy_every=5, heavy_scale=1e-3, fan_in_scaled=True) if grad == "philox" else {}
+    wl = workload.custom("max_w", _small_table(), W=W, chunk=chunk, grad=grad, grad_std=1e-3, **kw)
+    run(wl, 1, 2, error_storage=errors)
+
+
 # ---- 1-bit Adam variant ------------------------------------------------------
 
 def test_adam_variant_tiny_and_bert_mini():
