@@ -93,6 +93,16 @@ def test_odd_worker_count_and_large_w():
     run(bert_mini(W=37, chunk=512), 1, 2)
 
 
+def test_a_quarter_million_small_tensors():
+    """250,000 tensors of 1 to 8 elements (W = 2, C = 1024): every chunk holds
+    over a hundred tensors, far past the per-tile shared-memory slots of the
+    per-tensor ratio maximum, and the per-tensor kernels run a quarter of a
+    million CTAs or threads."""
+    rng = np.random.default_rng(21)
+    t = [(f"t{i}", (int(n),)) for i, n in enumerate(rng.integers(1, 9, 250_000))]
+    run(workload.custom("many_small", t, W=2, chunk=1024, grad_std=1e-3), 1, 2)
+
+
 def _small_table():
     return workload.bert_tensors(1, 32, 128, 300, max_pos=64) + [("tail", (37,))]
 
