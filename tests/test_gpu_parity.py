@@ -61,6 +61,18 @@ def test_bf16_gradients():
     run(wl, 3, 4)
 
 
+@pytest.mark.parametrize("chunk", [256, 512, 1024, 2048, 8192])
+def test_in_kernel_gradients_at_other_chunk_sizes(chunk):
+    """In-kernel gradients at the chunk sizes whose kernels draw them in the
+    compressing threads themselves (no draw warps): normal and Student-t
+    tensors, tiles that hold both kinds and tiles of only one."""
+    t = workload.bert_tensors(1, 64, 256, 700) + [("tail", (37,))]
+    wl = workload.custom("w5_philox", t, W=5, chunk=chunk, grad="philox", grad_std=1e-3,
+                         fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
+    assert wl.N % chunk != 0
+    run(wl, 2, 3)
+
+
 def test_in_kernel_philox_gradients_with_heavy_tails():
     """Gradients drawn inside the kernels (W=32), per-tensor std scaled by
     1/sqrt(fan_in), every fifth tensor Student-t(3)."""
