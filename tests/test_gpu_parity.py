@@ -73,6 +73,20 @@ def test_in_kernel_gradients_at_other_chunk_sizes(chunk):
     run(wl, 2, 3)
 
 
+@pytest.mark.parametrize("chunk", [256, 512, 1024, 2048, 4096, 8192])
+@pytest.mark.parametrize("grad", ["f32", "bf16", "philox"])
+@pytest.mark.parametrize("variant,errors", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_every_kernel_instantiation(variant, errors, grad, chunk):
+    """Every combination the dispatch can launch (method variant x error
+    storage x gradient kind x chunk size) on one small ragged table, W = 3:
+    each compiled kernel instantiation runs against the oracle at least
+    once."""
+    t = workload.bert_tensors(1, 32, 128, 300, max_pos=64) + [("tail", (37,))]
+    kw = dict(heavy_every=5, heavy_scale=1e-3, fan_in_scaled=True) if grad == "philox" else {}
+    wl = workload.custom("sweep", t, W=3, chunk=chunk, grad=grad, grad_std=1e-3, **kw)
+    run(wl, 1, 2, variant=variant, error_storage=errors)
+
+
 def test_in_kernel_philox_gradients_with_heavy_tails():
     """Gradients drawn inside the kernels (W=32), per-tensor std scaled by
     1/sqrt(fan_in), every fifth tensor Student-t(3)."""
