@@ -431,8 +431,8 @@ def run_reference(args, world, rank):
 def live_copy_gbs(gib=2, reps=5):
     """Bandwidth of a plain device-to-device copy on this GPU, measured now
     (bytes read + bytes written per second, best of reps, 2 GiB each way).
-    Context for the roofline fraction: the peak the fraction divides by was
-    measured once for the pool, and GB300s differ by a few percent."""
+    Context for the roofline fraction: the peak the fraction divides by is
+    a single stored measurement, and GB300s differ by a few percent."""
     import torch
     n = (gib << 30) // 4
     src = torch.empty(n, dtype=torch.float32, device="cuda").fill_(1.0)

@@ -70,9 +70,9 @@ def _bert_mini(W=4, chunk=1024):
     return workload.custom("bm", t, W=W, chunk=chunk, grad_std=1e-3)
 
 
-def _run_gpu_only(wl, n_warm, n_comp):
+def _run_gpu_only(wl, n_warm, n_comp, **opts):
     x = torch.from_numpy(workload.gen_params(wl)).cuda()
-    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    opt = pkg.OneBitLamb(x, layers_of(wl), wl.W, wl.chunk, **dict(wl.hp, **opts))
     ld = grad_ld(wl)
     t = 0
     for _ in range(n_warm):
@@ -86,27 +86,51 @@ def _run_gpu_only(wl, n_warm, n_comp):
     return opt, x
 
 
-def test_bitwise_deterministic():
-    wl = _bert_mini(W=6, chunk=2048)
-    a, xa = _run_gpu_only(wl, 3, 4)
-    b, xb = _run_gpu_only(wl, 3, 4)
+@pytest.mark.parametrize("shape", ["512x2", "three_cta_bf16err", "draw_warps"])
+def test_bitwise_deterministic(shape):
+    """Two runs of the same steps leave the same bits everywhere (with the
+    CPU parity this stands in for a race checker): the 512 x 2 tile, the
+    three-CTA shape with late server reads, and the in-kernel-gradient
+    kernel with its draw warps."""
+    opts = {}
+    if shape == "512x2":
+        wl = _bert_mini(W=6, chunk=2048)
+    elif shape == "three_cta_bf16err":
+        wl = _bert_mini(W=6, chunk=4096)
+        opts = dict(error_storage=1)
+    else:
+        t = workload.bert_tensors(1, 128, 512, 800)
+        wl = workload.custom("w32", t, W=32, chunk=4096, grad="philox", grad_std=1e-3,
+                             fan_in_scaled=True, heavy_every=5, heavy_scale=1e-3)
+    a, xa = _run_gpu_only(wl, 3, 4, **opts)
+    b, xb = _run_gpu_only(wl, 3, 4, **opts)
     assert torch.equal(xa.view(torch.int32), xb.view(torch.int32))
     assert torch.equal(a.workspace, b.workspace)
 
 
-def test_checkpoint_resume_is_bitwise():
-    wl = _bert_mini()
+def _same_bits(a, b):
+    it = torch.int32 if a.element_size() == 4 else torch.int16
+    return torch.equal(a.contiguous().view(it), b.contiguous().view(it))
+
+
+@pytest.mark.parametrize("chunk,variant,errors", [(1024, 0, 0), (4096, 0, 1), (4096, 1, 0), (2048, 1, 1)])
+def test_checkpoint_resume_is_bitwise(chunk, variant, errors):
+    """Save every state buffer after 3 warmup + 2 compression steps, restore
+    them into a new context, run 4 more: bit for bit the uninterrupted run,
+    for both method variants and both error storages."""
+    wl = _bert_mini(chunk=chunk)
+    opts = dict(variant=variant, error_storage=errors)
     ld = grad_ld(wl)
-    ref, xr = _run_gpu_only(wl, 3, 6)
+    ref, xr = _run_gpu_only(wl, 3, 6, **opts)
     # interrupted run: 3 warmup + 2 compression steps, save, restore, 4 more
-    a, xa = _run_gpu_only(wl, 3, 2)
+    a, xa = _run_gpu_only(wl, 3, 2, **opts)
     sa = a.state()
     saved = {k: v.clone() for k, v in sa.items() if isinstance(v, torch.Tensor)}
     counters = (sa["t"], sa["n_warmup"], sa["stage"])
     x_saved = xa.clone()
     del a
     xb = x_saved.clone()
-    b = pkg.OneBitLamb(xb, layers_of(wl), wl.W, wl.chunk, **wl.hp)
+    b = pkg.OneBitLamb(xb, layers_of(wl), wl.W, wl.chunk, **dict(wl.hp, **opts))
     sb = b.state()
     for k, v in saved.items():
         sb[k].copy_(v)
@@ -121,7 +145,7 @@ def test_checkpoint_resume_is_bitwise():
     sb = b.state()
     for k in ("m", "v", "v_fresh", "e_s", "e_w", "signs_w", "signs_s", "scale_w", "scale_s",
               "r_prev", "c_cur", "c_bar"):
-        assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
+        assert _same_bits(sb[k], sr[k]), k
 
 
 def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers():
