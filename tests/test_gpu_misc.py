@@ -148,17 +148,21 @@ def test_checkpoint_resume_is_bitwise(chunk, variant, errors):
         assert _same_bits(sb[k], sr[k]), k
 
 
-def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers():
+@pytest.mark.parametrize("chunk,variant,errors", [(1024, 0, 0), (4096, 0, 1), (4096, 1, 0)])
+def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers(chunk, variant, errors):
     """Failure path without a GPU fault: the first CTA leaves out one of its
     shared-memory bulk copies, so its bounded wait for it runs out.  The step
     reports LAMB1B_ERR_TIMEOUT, the context stays usable, and restoring the
     state saved before the step continues bit for bit like an uninterrupted
     run.  Skipped copies: the first tile's momentum, a worker's gradient, a
-    worker's error, the server error, the fresh second moment."""
-    wl = _bert_mini()
+    worker's error, the server error, and for 1-bit LAMB the fresh second
+    moment (one of the two slots its server holds to the end of the tile).
+    Shapes: a 7-slot ring, and the three-CTA shape's 4-slot ring."""
+    wl = _bert_mini(chunk=chunk)
+    opts = dict(variant=variant, error_storage=errors)
     ld = grad_ld(wl)
-    ref, xr = _run_gpu_only(wl, 3, 4)
-    a, xa = _run_gpu_only(wl, 3, 2)
+    ref, xr = _run_gpu_only(wl, 3, 4, **opts)
+    a, xa = _run_gpu_only(wl, 3, 2, **opts)
     sa = a.state()
     saved = {k: v.clone() for k, v in sa.items() if isinstance(v, torch.Tensor)}
     counters = (sa["t"], sa["n_warmup"], sa["stage"])
@@ -167,7 +171,8 @@ def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers():
     # copy positions of the first tile: 0 momentum, 1 + 2w gradient of worker
     # w, 2 + 2w its error, 1 + 2W server error, 2 + 2W frozen v, 3 + 2W v_fresh
     W = wl.W
-    for skip in (0, 5, 2 * W, 1 + 2 * W, 3 + 2 * W):
+    skips = (0, 5, 2 * W, 1 + 2 * W) + (() if variant else (3 + 2 * W,))
+    for skip in skips:
         a.set_fault_injection(skip, 2000)
         a.compress_step(device_grads(wl, t, ld))
         with pytest.raises(pkg.Lamb1bError) as e:
@@ -189,7 +194,7 @@ def test_copy_wait_timeout_is_reported_and_a_checkpoint_recovers():
     sr, sb = ref.state(), a.state()
     for k in ("m", "v", "v_fresh", "e_s", "e_w", "signs_w", "signs_s", "scale_w", "scale_s",
               "r_prev", "c_cur", "c_bar"):
-        assert torch.equal(sb[k].view(torch.int32), sr[k].view(torch.int32)), k
+        assert _same_bits(sb[k], sr[k]), k
 
 
 def test_copy_wait_timeout_with_draw_warps_recovers():
