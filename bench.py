@@ -112,6 +112,28 @@ def update_kernel_bytes(wl):
     return wl.N * 12.125 + 4.0 * wl.K
 
 
+def warmup_kernel_bytes(wl, variant="lamb"):
+    """Warmup moments kernel: per parameter the W gradients, m and v read
+    and written, and (1-bit LAMB, for the trust ratio's norms) x read."""
+    return wl.N * (wl.W * grad_bytes(wl) + (16.0 if variant == "adam" else 20.0))
+
+
+def warmup_stage_line(wl, variant, N, peak, warm_ms, kern_ms, layer_ms, upd_ms):
+    """The warmup stage's per-step times (the first step, which builds
+    nothing different but starts cold, is left out when there are more) and
+    its two streaming kernels against the same peak as the compression
+    stage (the warmup update moves m, v and x read, x written: 16 B)."""
+    def avg(v):
+        return statistics.mean(v[1:] or v)
+    mk, uk = avg(kern_ms), avg(upd_ms)
+    mb, ub = warmup_kernel_bytes(wl, variant), 16.0 * wl.N
+    return {"ms_per_step": avg(warm_ms), "moments_kernel_ms": mk, "per_tensor_ms": avg(layer_ms),
+            "update_ms": uk, "params_per_s": N / (avg(warm_ms) / 1e3),
+            "moments_gbs": mb / (mk / 1e3) / 1e9, "moments_frac_of_peak": mb / (mk / 1e3) / 1e9 / peak,
+            "update_gbs": ub / (uk / 1e3) / 1e9, "update_frac_of_peak": ub / (uk / 1e3) / 1e9 / peak,
+            "steps": len(warm_ms)}
+
+
 def step_bytes(wl, variant="lamb", errors="f32"):
     return fused_kernel_bytes(wl, variant, errors) + update_kernel_bytes(wl)
 
@@ -486,7 +508,7 @@ def run_ours(args, world, rank, local):
 
     # warmup stage (LAMB), timed per step for information
     t = 0
-    warm_ms, warm_kernel_ms, warm_layer_ms = [], [], []
+    warm_ms, warm_kernel_ms, warm_layer_ms, warm_upd_ms = [], [], [], []
     n_warm_stage = wl.warmup_steps if args.warmup_stage_steps < 0 else args.warmup_stage_steps
     for _ in range(n_warm_stage):
         regen(t)
@@ -497,6 +519,7 @@ def run_ours(args, world, rank, local):
         warm_ms.append(ev[0].elapsed_time(ev[3]))
         warm_kernel_ms.append(ev[0].elapsed_time(ev[1]))
         warm_layer_ms.append(ev[1].elapsed_time(ev[2]))
+        warm_upd_ms.append(ev[2].elapsed_time(ev[3]))
         t += 1
     opt.freeze_variance()
     for _ in range(args.warmup):
@@ -616,11 +639,8 @@ def run_ours(args, world, rank, local):
                  "ms_p50": float(np.percentile(step_ms, 50)),
                  "ms_p90": float(np.percentile(step_ms, 90)),
                  "worker_elements_per_s": W * value, "wall_s": wall},
-        "warmup_stage": ({"ms_per_step": statistics.mean(warm_ms[1:] or warm_ms),
-                          "moments_kernel_ms": statistics.mean(warm_kernel_ms[1:] or warm_kernel_ms),
-                          "per_tensor_ms": statistics.mean(warm_layer_ms[1:] or warm_layer_ms),
-                          "params_per_s": N / (statistics.mean(warm_ms[1:] or warm_ms) / 1e3),
-                          "steps": len(warm_ms)} if warm_ms else None),
+        "warmup_stage": (warmup_stage_line(wl, args.variant, N, peak, warm_ms, warm_kernel_ms,
+                                           warm_layer_ms, warm_upd_ms) if warm_ms else None),
         "gpu_launches": (2 if args.variant == "adam" else 3) * args.steps,
         "layer_stats": layer_stats,
         "clocks": clocks,
