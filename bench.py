@@ -574,7 +574,8 @@ def run_ours(args, world, rank, local):
                         "achieved": t_ips / 1e12, "peak": ISSUE_PEAK / 1e12,
                         "unit": "T thread-inst/s", "frac": t_ips / ISSUE_PEAK,
                         "peak_source": "152 SMs x 4 schedulers x 32 lanes x 2070 MHz",
-                        "traffic": None, "thread_inst_per_launch": inst, "kernel_ms": k_avg,
+                        "traffic": traffic, "traffic_source": traffic_source,
+                        "thread_inst_per_launch": inst, "kernel_ms": k_avg,
                         "hbm": {"achieved": achieved, "peak": peak, "unit": "GB/s",
                                 "frac": achieved / peak, "alg_bytes_per_launch": kb,
                                 "live_copy_gbs": copy_now}}
