@@ -129,6 +129,9 @@ def warmup_stage_line(wl, variant, N, peak, warm_ms, kern_ms, layer_ms, upd_ms):
     mb, ub = warmup_kernel_bytes(wl, variant), 16.0 * wl.N
     return {"ms_per_step": avg(warm_ms), "moments_kernel_ms": mk, "per_tensor_ms": avg(layer_ms),
             "update_ms": uk, "params_per_s": N / (avg(warm_ms) / 1e3),
+            # in-kernel gradients: the moments kernel draws W values per element
+            # and is bound by that arithmetic, not by HBM
+            "moments_bound": "alu" if wl.grad == "philox" else "hbm",
             "moments_gbs": mb / (mk / 1e3) / 1e9, "moments_frac_of_peak": mb / (mk / 1e3) / 1e9 / peak,
             "update_gbs": ub / (uk / 1e3) / 1e9, "update_frac_of_peak": ub / (uk / 1e3) / 1e9 / peak,
             "steps": len(warm_ms)}
